@@ -1,0 +1,439 @@
+"""Benchmark of the compressed-KV sparse-attention decode step on GB300.
+
+One step = CSA indexer score + exact top-512 over all N compressed rows of
+one layer, then sparse attention of the 64-head decode query over the 512
+selected packed KV rows (batch 1).  Default workload: the long decode layer,
+N = 1,048,576 rows (68-byte MXFP4 indexer rows, 583-byte KV rows, 64 indexer
+heads x 128, 64 attention heads x 512), synthetic N(0,1) data packed by the
+library's own cache writer.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs (one graph per layer cache), bracketed by a barrier and a device
+synchronise, timed with CUDA events on the launching stream.  Inputs larger
+than L2: the steps rotate over L layer caches (L x 71.3 MB of indexer rows
+> 4 x the 129 MB L2), so every step streams its rows from HBM.
+
+Printed: one JSON line (rank 0).  `value` is compressed rows scored per second
+over the whole job; `roofline` is the dominant kernel (the scorer entry
+point) timed on its own over K graph replays; `e2e` times the same step
+through the public API from pinned host buffers (append of the new row,
+score, attention, result copied back); `cpu_baseline` is the float64 oracle
+on the host cores on a bounded sample.  `--impl reference` times the oracle
+alone (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn step latency (µs/layer) & compressed rows/s vs N; achieved HBM GB/s"
+WORKLOADS = {"tiny": 4096, "mid": 131072, "long": 1048576}
+K_TOP = 512
+HEADS = 64
+FALLBACK_HBM_GBS = 6800.0
+
+
+def step_bytes(n):
+    """Algorithmic HBM bytes of one decode step (what the method must move)."""
+    return scorer_bytes(n) + attn_bytes()
+
+
+def scorer_bytes(n):
+    # indexer rows + bf16 query + f32 weights + top-k indices and scores written
+    return 68 * n + HEADS * 128 * 2 + HEADS * 4 + K_TOP * (4 + 4)
+
+
+def attn_bytes():
+    # gathered KV rows + index list + bf16 query + bf16 output + lse
+    return K_TOP * 583 + K_TOP * 4 + HEADS * 512 * 2 + HEADS * 512 * 2 + HEADS * 4
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_hash():
+    csrc = os.path.join(ROOT, "compressed_kv_sparse_csa_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except Exception:
+        return None, None
+    ent = rec.get(kernel_name)
+    if not ent or ent.get("sources_hash") != kernel_sources_hash():
+        return None, None
+    return ent.get("dram_bytes_per_launch_full_size"), ent.get("note")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ds4x_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the float64 oracle as it stands
+# ---------------------------------------------------------------------------
+
+def oracle_step_sample(n_rows, seed=1002):
+    """Time one oracle decode step (score + top-512 + attention) over the
+    first n_rows of the long-decode workload's distribution.  Returns seconds."""
+    import numpy as np
+
+    from oracle import codecs as C
+    from oracle import indexer as I
+    from oracle.attention import sparse_attn_decode
+    from synth import decode_case
+
+    case = decode_case(n_rows, seed)
+    idx_rows = C.pack_idx_rows(case["idx_in"])
+    t0 = time.perf_counter()
+    idx, _, _ = I.score_topk(idx_rows, case["q_idx"], case["w"], K_TOP)
+    t1 = time.perf_counter()
+    # packing is not part of the step: pack just the selected KV rows, untimed
+    kv_sel = C.pack_kv_rows(case["kv_in"][idx])
+    t2 = time.perf_counter()
+    sparse_attn_decode(kv_sel, np.arange(idx.shape[0]), case["q_attn"], 1.0 / math.sqrt(512.0))
+    return (t1 - t0) + (time.perf_counter() - t2)
+
+
+def run_oracle_subprocess(n_rows, reps):
+    """Run the oracle in a single-threaded child process; returns list of seconds."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; import json; "
+            f"print(json.dumps([bench.oracle_step_sample({n_rows}, seed=1002 + i) for i in range({reps})]))")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(n_rows=262144, reps=5):
+    secs = run_oracle_subprocess(n_rows, reps)
+    t = sorted(secs)[len(secs) // 2]
+    return {"value": n_rows / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"median of {reps} oracle steps (score + top-512 + attention) over {n_rows} rows of the "
+                      f"long-decode distribution, numpy float64, 1 thread; {t:.2f} s each"}
+
+
+def reference_arm(args, workload, n):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    # size each step's sample so the whole run stays within about two minutes
+    probe = run_oracle_subprocess(8192, 1)[0]
+    rate = 8192 / probe
+    total_steps = args.steps + args.warmup
+    sample = int(max(1024, min(262144, rate * 100.0 / max(1, total_steps))) // 1024 * 1024)
+    secs = run_oracle_subprocess(sample, total_steps)
+    timed = secs[args.warmup:]
+    t = sum(timed)
+    value = sample * len(timed) / t
+    line = {"metric": METRIC, "value": value, "unit": "compressed rows/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload, "n_rows": n, "top_k": K_TOP, "sample_rows_per_step": sample},
+            "cpu_baseline": {"value": value, "unit": "compressed rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{sample} rows per step of the {workload} decode distribution, "
+                                       "numpy float64 oracle, 1 thread"},
+            "e2e": {"value": value, "unit": "compressed rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    n = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, args.workload, n)
+        return
+
+    import torch
+
+    from compressed_kv_sparse_csa_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    L = args.layers
+    scale = 1.0 / math.sqrt(512.0)
+
+    # ---- resident inputs: L layer caches packed by the library's cache writer
+    gen = torch.Generator(device=dev)
+    layers = []
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            gen.manual_seed(1002 * 1000 + 97 * rank + l)
+            idx_rows = torch.empty(n * 68, dtype=torch.uint8, device=dev)
+            kv_rows = torch.empty(n * 583, dtype=torch.uint8, device=dev)
+            chunk = 1 << 18
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                idx_in = torch.randn((b - a, 128), generator=gen, device=dev)
+                kv_in = torch.randn((b - a, 512), generator=gen, device=dev)
+                B.ds4x_cache_append(kv_rows, idx_rows, a, kv_in, idx_in, stream=stream)
+            q_idx = torch.randn((HEADS, 128), generator=gen, device=dev).to(torch.bfloat16)
+            w = torch.rand(HEADS, generator=gen, device=dev) / 8
+            q_attn = torch.randn((HEADS, 512), generator=gen, device=dev).to(torch.bfloat16)
+            layers.append({"idx_rows": idx_rows, "kv_rows": kv_rows, "q_idx": q_idx, "w": w, "q_attn": q_attn,
+                           "out_idx": torch.empty(K_TOP, dtype=torch.int32, device=dev),
+                           "out_score": torch.empty(K_TOP, dtype=torch.float32, device=dev),
+                           "out": torch.empty((HEADS, 512), dtype=torch.bfloat16, device=dev)})
+        ws_s = torch.empty(B.ds4x_index_score_topk_workspace(n, K_TOP), dtype=torch.uint8, device=dev)
+        ws_a = torch.empty(B.ds4x_sparse_attn_decode_workspace(K_TOP), dtype=torch.uint8, device=dev)
+        B.ds4x_workspace_init(ws_s, stream=stream)
+        B.ds4x_workspace_init(ws_a, stream=stream)
+    stream.synchronize()
+
+    def step(l, score_only=False):
+        c = layers[l]
+        B.ds4x_index_score_topk(c["idx_rows"], n, c["q_idx"], c["w"], K_TOP, c["out_idx"], c["out_score"], ws_s,
+                                stream=stream)
+        if not score_only:
+            B.ds4x_sparse_attn_decode(c["kv_rows"], n, c["out_idx"], K_TOP, c["q_attn"], scale, c["out"], None,
+                                      ws_a, stream=stream)
+
+    launches_per_step = {"score": 2, "attn": 2}  # kernels each entry point launches (two-stage scorer)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i % L)
+    stream.synchronize()
+
+    def capture(score_only):
+        graphs = []
+        for l in range(L):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(l, score_only)
+            graphs.append(g)
+        return graphs
+
+    step_graphs = capture(False)
+    score_graphs = capture(True)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def timed(graphs, k):
+        with torch.cuda.stream(stream):
+            for g in graphs:  # untimed replay of each graph once
+                g.replay()
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            e0.record(stream)
+            for i in range(k):
+                graphs[i % L].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1)  # ms
+
+    with ClockSampler(local) as clk:
+        ms_total = timed(step_graphs, args.steps)
+    clocks = clk.summary()
+    ms_score = timed(score_graphs, args.steps)
+
+    # ---- end to end through the public API, host buffers, copies inside
+    e2e_steps = min(args.steps, 500)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_kv = pin(torch.randn((1, 512)))
+    h_idx = pin(torch.randn((1, 128)))
+    h_q = pin(layers[0]["q_idx"])
+    h_w = pin(layers[0]["w"])
+    h_qa = pin(layers[0]["q_attn"])
+    h_out = torch.empty((HEADS, 512), dtype=torch.bfloat16).pin_memory()
+    h_oidx = torch.empty(K_TOP, dtype=torch.int32).pin_memory()
+    d_kv = torch.empty((1, 512), device=dev)
+    d_idx = torch.empty((1, 128), device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_kv, h_idx, h_q, h_w, h_qa))
+    d2h = h_out.numel() * h_out.element_size() + h_oidx.numel() * h_oidx.element_size()
+
+    def e2e_step(l):
+        c = layers[l]
+        d_kv.copy_(h_kv, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        c["q_idx"].copy_(h_q, non_blocking=True)
+        c["w"].copy_(h_w, non_blocking=True)
+        c["q_attn"].copy_(h_qa, non_blocking=True)
+        B.ds4x_cache_append(c["kv_rows"], c["idx_rows"], n - 1, d_kv, d_idx, stream=stream)
+        step(l)
+        h_out.copy_(c["out"], non_blocking=True)
+        h_oidx.copy_(c["out_idx"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i % L)
+        stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i % L)
+        e1.record(stream)
+        stream.synchronize()
+        barrier()
+        ms_e2e = max(e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0))
+
+    ms_step = ms_total / args.steps
+    ms_sc = ms_score / args.steps
+    ms_e2e_step = ms_e2e / e2e_steps
+    if dist is not None:
+        t = torch.tensor([ms_step, ms_sc, ms_e2e_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_sc, ms_e2e_step = t.tolist()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    sb = scorer_bytes(n)
+    achieved = sb / (ms_sc * 1e-3) / 1e9
+    traffic, tnote = recorded_traffic("ds4x_index_score_topk")
+    line = {
+        "metric": METRIC,
+        "value": world * n / (ms_step * 1e-3),
+        "unit": "compressed rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16-in/fp32-acc (MXFP4 + E4M3/FP16 packed rows)",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} decode, batch 1, one layer",
+                   "n_rows": n, "top_k": K_TOP, "indexer_heads": HEADS, "attn_heads": HEADS,
+                   "layer_caches_rotated": L,
+                   "l2": f"inputs larger than L2: {L} layer caches x {68 * n / 1e6:.1f} MB indexer rows rotated",
+                   "us_per_layer": ms_step * 1e3,
+                   "achieved_step_gbs": step_bytes(n) / (ms_step * 1e-3) / 1e9,
+                   "step_bytes": step_bytes(n),
+                   "step_roofline_frac": (step_bytes(n) / (ms_step * 1e-3) / 1e9) / peak,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "ds4x_index_score_topk", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "traffic_note": tnote, "algorithmic_bytes_per_launch": sb, "us_per_launch": ms_sc * 1e3},
+        "e2e": {"value": world * n / (ms_e2e_step * 1e-3), "unit": "compressed rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": ms_e2e_step},
+        "gpu_launches": args.steps * (launches_per_step["score"] + launches_per_step["attn"]),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline()
+        except Exception as e:  # report, never fake
+            line["cpu_baseline"] = {"value": None, "error": str(e)[-300:]}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+"""ctypes binding of libds4x (include/ds4x.h): argument marshalling only.
+
+Every function takes torch tensors on the current CUDA device, checks their
+dtype / shape / contiguity, and passes raw device pointers and the current
+stream to the C entry point of the same name.  All computation runs in the
+library's CUDA kernels; there is no Python or CPU fallback.  A missing or
+unloadable library raises at first use.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+_LIB = None
+
+_c_i32 = ctypes.c_int32
+_c_i64 = ctypes.c_int64
+_c_size = ctypes.c_size_t
+_c_p = ctypes.c_void_p
+_c_f32 = ctypes.c_float
+
+_SIGNATURES = {
+    "ds4x_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "ds4x_abi_version": (ctypes.c_int, []),
+    "ds4x_cache_bytes": (_c_i64, [_c_i64]),
+    "ds4x_workspace_init": (ctypes.c_int, [_c_p, _c_size, _c_p]),
+    "ds4x_workspace_status": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(_c_i32)]),
+    "ds4x_cache_append": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p]),
+    "ds4x_index_score_topk_workspace": (_c_size, [_c_i64, _c_i32]),
+    "ds4x_index_score_topk": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p]),
+    "ds4x_sparse_attn_decode_workspace": (_c_size, [_c_i32]),
+    "ds4x_sparse_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p, _c_size, _c_p]),
+}
+
+
+class Ds4xError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({status_str(status)})")
+
+
+def lib():
+    """Load libds4x.so (built by __graft_entry__.build()); raise if absent."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def status_str(status: int) -> str:
+    return lib().ds4x_status_str(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, dtype, name, numel=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+
+
+def _call(fn, *args):
+    st = getattr(lib(), fn)(*args)
+    if st != 0:
+        raise Ds4xError(fn, st)
+
+
+def ds4x_abi_version() -> int:
+    return lib().ds4x_abi_version()
+
+
+def ds4x_cache_bytes(context_tokens: int) -> int:
+    return lib().ds4x_cache_bytes(int(context_tokens))
+
+
+def ds4x_workspace_init(ws, stream=None):
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_workspace_init", _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_workspace_status(ws, stream=None) -> int:
+    _check(ws, torch.uint8, "ws")
+    out = _c_i32(0)
+    _call("ds4x_workspace_status", _ptr(ws), _stream(stream), ctypes.byref(out))
+    return out.value
+
+
+def ds4x_cache_append(kv_rows, idx_rows, pos, kv_in, idx_in, stream=None):
+    """Pack kv_in f32 [n, 512] / idx_in f32 [n, 128] into rows [pos, pos+n)
+    of kv_rows u8 [cap, 583] / idx_rows u8 [cap, 68] (either may be None)."""
+    _check(kv_rows, torch.uint8, "kv_rows", allow_none=True)
+    _check(idx_rows, torch.uint8, "idx_rows", allow_none=True)
+    _check(kv_in, torch.float32, "kv_in", allow_none=kv_rows is None)
+    _check(idx_in, torch.float32, "idx_in", allow_none=idx_rows is None)
+    src = kv_in if kv_in is not None else idx_in
+    n = src.shape[0]
+    cap = (kv_rows if kv_rows is not None else idx_rows).numel() // (583 if kv_rows is not None else 68)
+    if kv_rows is not None and idx_rows is not None and idx_rows.numel() // 68 != cap:
+        raise ValueError("kv_rows and idx_rows hold different row counts")
+    _call("ds4x_cache_append", _ptr(kv_rows), _ptr(idx_rows), cap, int(pos), _ptr(kv_in), _ptr(idx_in), n,
+          _stream(stream))
+
+
+def ds4x_index_score_topk_workspace(n_rows: int, k: int) -> int:
+    return lib().ds4x_index_score_topk_workspace(int(n_rows), int(k))
+
+
+def ds4x_index_score_topk(idx_rows, n_rows, q_bf16, w, k, out_idx, out_score, ws, stream=None):
+    """Score n_rows packed indexer rows and write the exact top-k indices
+    (and scores, if out_score is given) in score-descending order."""
+    _check(idx_rows, torch.uint8, "idx_rows", numel=int(n_rows) * 68)
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=64 * 128)
+    _check(w, torch.float32, "w", numel=64)
+    _check(out_idx, torch.int32, "out_idx", numel=int(k))
+    _check(out_score, torch.float32, "out_score", numel=int(k), allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_index_score_topk", _ptr(idx_rows), int(n_rows), _ptr(q_bf16), _ptr(w), int(k), _ptr(out_idx),
+          _ptr(out_score), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_sparse_attn_decode_workspace(k: int) -> int:
+    return lib().ds4x_sparse_attn_decode_workspace(int(k))
+
+
+def ds4x_sparse_attn_decode(kv_rows, n_rows, idx, k, q_bf16, softmax_scale, out_bf16, lse, ws, stream=None):
+    """Decode attention of q_bf16 [64, 512] over the k rows listed in idx."""
+    _check(kv_rows, torch.uint8, "kv_rows", numel=int(n_rows) * 583)
+    _check(idx, torch.int32, "idx", numel=int(k))
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=64 * 512)
+    _check(out_bf16, torch.bfloat16, "out_bf16", numel=64 * 512)
+    _check(lse, torch.float32, "lse", numel=64, allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_sparse_attn_decode", _ptr(kv_rows), int(n_rows), _ptr(idx), int(k), _ptr(q_bf16),
+          float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))

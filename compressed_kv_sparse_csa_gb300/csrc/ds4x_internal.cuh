@@ -1,0 +1,81 @@
+// Internal declarations shared by the CUDA translation units of libds4x.
+// Not part of the ABI; see include/ds4x.h for the public contract.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "ds4x.h"
+
+namespace ds4x {
+
+// ---------------------------------------------------------------------------
+// Workspace header: the first 256 bytes of every workspace.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  int32_t status;        // DS4X_OK / DS4X_EDEVICE / DS4X_ETIMEOUT (sticky)
+  uint32_t ticket;       // arrival counter of the fused scorer (self-resetting)
+  uint32_t fallback;     // number of scorer calls that took the slow merge
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+constexpr size_t kWsHeaderBytes = 256;
+
+// ---------------------------------------------------------------------------
+// Sortable 64-bit (score, index) keys: larger key == earlier in the top-k.
+// High word: the score's bits mapped to an unsigned total order (-0 first
+// canonicalised to +0).  Low word: ~index, so the lower index wins a tie.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t float_to_ordered(float s) {
+  uint32_t u = __float_as_uint(s == 0.0f ? 0.0f : s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_to_float(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ uint64_t make_key(float s, uint32_t idx) {
+  return (uint64_t(float_to_ordered(s)) << 32) | uint64_t(~idx);
+}
+__device__ __forceinline__ int32_t key_index(uint64_t key) {
+  return int32_t(~uint32_t(key & 0xffffffffu));
+}
+__device__ __forceinline__ float key_score(uint64_t key) {
+  return ordered_to_float(uint32_t(key >> 32));
+}
+
+// Raises a kernel's dynamic shared-memory limit, once per device.
+template <typename Kernel>
+cudaError_t set_max_smem_once(Kernel *kernel, int bytes, std::atomic<uint64_t> &done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (host).  Each returns a cudaError_t from cudaGetLastError().
+// ---------------------------------------------------------------------------
+cudaError_t launch_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t pos,
+                                const float *kv_in, const float *idx_in, int64_t n,
+                                cudaStream_t stream);
+
+// Two-stage scorer: full key array, then a single-CTA radix select.
+size_t score_two_stage_ws_bytes(int64_t n_rows);
+cudaError_t launch_score_two_stage(const uint8_t *idx_rows, int64_t n_rows,
+                                   const uint16_t *q, const float *w, int32_t k,
+                                   int32_t *out_idx, float *out_score, void *ws,
+                                   cudaStream_t stream);
+
+size_t attn_decode_ws_bytes(int32_t k);
+cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
+                               int32_t k, const uint16_t *q, float scale, uint16_t *out,
+                               float *lse, void *ws, cudaStream_t stream);
+
+}  // namespace ds4x

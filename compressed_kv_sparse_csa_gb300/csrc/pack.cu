@@ -1,0 +1,116 @@
+// Cache writer: quantise and pack new compressed rows into the 583-byte KV
+// row and the 68-byte MXFP4 indexer row (DS4X README, "Packed cache ABI").
+//
+// One warp per row.  Scale rule per block: e = least integer with
+// amax <= emax * 2^e (exact via frexp), scale byte e + 127; elements are
+// x = v * 2^-e (exact power-of-two scaling) converted with the hardware
+// round-to-nearest-even E2M1 / E4M3 converters; RoPE values go to FP16 RNE.
+#include <cuda_fp16.h>
+
+#include "ds4x_internal.cuh"
+
+namespace ds4x {
+namespace {
+
+// Least integer e with amax <= emax * 2^e, where emax = g * 2^G (0.5 <= g < 1):
+// with amax = f * 2^F, e = F - G when f <= g, else F - G + 1.
+__device__ __forceinline__ int block_exponent(float amax, float g, int G) {
+  if (amax == 0.0f) return 0;
+  int F;
+  const float f = frexpf(amax, &F);
+  const int e = F - G + (f > g ? 1 : 0);
+  return max(-127, min(127, e));
+}
+
+// 2^-e as a float, for e in [-127, 126] (every exponent a finite block can have).
+__device__ __forceinline__ float pow2_neg(int e) {
+  return __uint_as_float(uint32_t(127 - e) << 23);
+}
+
+// Two floats -> one byte of two E2M1 codes: `lo` in bits 0-3, `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r) : "f"(hi), "f"(lo));
+  return r & 0xffu;
+}
+
+// Two floats -> two E4M3 codes: `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+cache_append_kernel(uint8_t *__restrict__ kv_rows, uint8_t *__restrict__ idx_rows, int64_t pos,
+                    const float *__restrict__ kv_in, const float *__restrict__ idx_in,
+                    int64_t n) {
+  __shared__ __align__(16) uint32_t stage[kWarps][(DS4X_KV_ROW_BYTES + 3) / 4];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t row = int64_t(blockIdx.x) * kWarps + warp;
+  if (row >= n) return;
+
+  if (idx_rows != nullptr) {
+    // lane owns elements 4*lane .. 4*lane+3, all in 32-value block lane/8
+    const float4 v = reinterpret_cast<const float4 *>(idx_in + row * DS4X_IDX_DIM)[lane];
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int e = block_exponent(amax, 0.75f, 3);  // 6 = 0.75 * 2^3
+    const float s = pow2_neg(e);
+    const uint32_t b0 = cvt_e2m1x2(v.y * s, v.x * s);
+    const uint32_t b1 = cvt_e2m1x2(v.w * s, v.z * s);
+    uint8_t *dst = idx_rows + (pos + row) * DS4X_IDX_ROW_BYTES;
+    dst[2 * lane] = uint8_t(b0);
+    dst[2 * lane + 1] = uint8_t(b1);
+    if ((lane & 7) == 0) dst[DS4X_IDX_DIM / 2 + (lane >> 3)] = uint8_t(e + 127);
+  }
+
+  if (kv_rows != nullptr) {
+    // stage the row in shared memory with aligned 16/32-bit stores, then copy
+    // it out byte-wise (KV rows are 583 bytes, so row starts are unaligned)
+    uint32_t *st32 = stage[warp];
+    uint16_t *st16 = reinterpret_cast<uint16_t *>(st32);
+    uint8_t *st8 = reinterpret_cast<uint8_t *>(st32);
+    const float *src = kv_in + row * DS4X_KV_DIM;
+#pragma unroll
+    for (int b = 0; b < DS4X_KV_NOPE / DS4X_KV_BLOCK; ++b) {
+      const float2 v = reinterpret_cast<const float2 *>(src + b * DS4X_KV_BLOCK)[lane];
+      const float amax = warp_max(fmaxf(fabsf(v.x), fabsf(v.y)), 32);
+      const int e = block_exponent(amax, 0.875f, 9);  // 448 = 0.875 * 2^9
+      const float s = pow2_neg(e);
+      st16[b * (DS4X_KV_BLOCK / 2) + lane] = uint16_t(cvt_e4m3x2(v.y * s, v.x * s));
+      if (lane == 0) st8[DS4X_KV_NOPE + 2 * DS4X_KV_ROPE + b] = uint8_t(e + 127);
+    }
+    const float2 r = reinterpret_cast<const float2 *>(src + DS4X_KV_NOPE)[lane];
+    const uint32_t h0 = __half_as_ushort(__float2half_rn(r.x));
+    const uint32_t h1 = __half_as_ushort(__float2half_rn(r.y));
+    st32[DS4X_KV_NOPE / 4 + lane] = h0 | (h1 << 16);  // little-endian FP16 pair
+    __syncwarp();
+    uint8_t *dst = kv_rows + (pos + row) * DS4X_KV_ROW_BYTES;
+    for (int i = lane; i < DS4X_KV_ROW_BYTES; i += 32) dst[i] = st8[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t pos,
+                                const float *kv_in, const float *idx_in, int64_t n,
+                                cudaStream_t stream) {
+  const int64_t blocks = (n + kWarps - 1) / kWarps;
+  cache_append_kernel<<<dim3(unsigned(blocks)), kWarps * 32, 0, stream>>>(kv_rows, idx_rows, pos,
+                                                                          kv_in, idx_in, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ds4x

@@ -1,0 +1,205 @@
+/*
+ * ds4x.h -- C ABI of the GB300 (sm_103a) compressed-KV sparse-attention
+ * (CSA) decode path.
+ *
+ * The path (DS4X README, "What DS4X changes" and "Optimization details"):
+ *   1. a CSA indexer scores every compressed history row, reading packed
+ *      68-byte MXFP4 rows directly;
+ *   2. an exact top-k (k <= 512) picks rows under the float total order of
+ *      the score with the lower row index winning ties;
+ *   3. sparse attention runs over the selected 583-byte packed KV rows.
+ * A cache writer quantises and packs new rows into both formats.
+ *
+ * Row formats (DS4X README, "Packed cache ABI"):
+ *   KV row (583 B)      = 448 E4M3FN codes (element order)
+ *                       + 64 FP16 RoPE values, little-endian (128 B)
+ *                       + 7 UE8M0 scales, one per 64-value non-RoPE block
+ *   indexer row (68 B)  = 128 E2M1 codes, two per byte, even element in the
+ *                         low nibble (64 B)
+ *                       + 4 UE8M0 scales, one per 32-value block
+ *   A UE8M0 byte b stands for 2^(b - 127).  Row i of an array of n rows
+ *   starts at byte i * 583 (KV) or i * 68 (indexer); arrays are contiguous.
+ *
+ * Conventions for every entry point below:
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, and must be
+ *     16-byte aligned.  The caller owns all memory (rows, inputs, outputs and
+ *     workspace); the library allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise it.
+ *   - Calls return DS4X_OK (0) or a negative status.  Arguments are checked
+ *     on the host before anything is launched; a failed check launches
+ *     nothing and leaves every buffer untouched.  DS4X_ECUDA reports a
+ *     launch failure (the CUDA error is left for cudaGetLastError to read).
+ *     No call traps, asserts or throws across the ABI.
+ *   - Inputs must be finite; NaN or infinite inputs give unspecified (but
+ *     memory-safe) results.
+ *   - bfloat16 data is passed as uint16_t bit patterns.
+ *   - The library runs only on compute capability 10.3 (GB300);
+ *     anything else returns DS4X_EARCH.
+ */
+#ifndef DS4X_H
+#define DS4X_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st *ds4x_stream_t;
+
+#define DS4X_ABI_VERSION 1
+
+#define DS4X_KV_ROW_BYTES 583
+#define DS4X_KV_DIM 512
+#define DS4X_KV_NOPE 448
+#define DS4X_KV_ROPE 64
+#define DS4X_KV_BLOCK 64
+#define DS4X_IDX_ROW_BYTES 68
+#define DS4X_IDX_DIM 128
+#define DS4X_IDX_BLOCK 32
+#define DS4X_IDX_HEADS 64
+#define DS4X_ATTN_HEADS 64
+#define DS4X_TOPK_MAX 512
+
+enum {
+  DS4X_OK = 0,
+  DS4X_EINVAL = -1,     /* null or misaligned pointer, bad size or k      */
+  DS4X_ERANGE = -2,     /* pos / n outside the cache capacity              */
+  DS4X_EWORKSPACE = -3, /* workspace smaller than the *_workspace() size   */
+  DS4X_EARCH = -4,      /* current device is not compute capability 10.3   */
+  DS4X_ECUDA = -5,      /* a CUDA runtime call or launch failed            */
+  DS4X_ETIMEOUT = -6,   /* device status: a bounded wait gave up           */
+  DS4X_EDEVICE = -7     /* device status: kernel-detected bad input        */
+};
+
+/* Static text for a status code (host pointer, never NULL). */
+const char *ds4x_status_str(int status);
+
+/* DS4X_ABI_VERSION of the built library. */
+int ds4x_abi_version(void);
+
+/*
+ * Persistent packed KV + indexer bytes a DeepSeek-V4-Flash context of
+ * `context_tokens` tokens needs (DS4X README, "Packed cache ABI": 43 layers
+ * with a 256-row raw ring, 21 CSA layers at ratio 4 holding KV and indexer
+ * rows, 20 HCA layers at ratio 128 holding KV rows):
+ *   43*256*583 + 21*(L/4 + 2)*(583 + 68) + 20*(L/128 + 2)*583.
+ * Host-only arithmetic.  Returns -1 for a negative argument.
+ */
+int64_t ds4x_cache_bytes(int64_t context_tokens);
+
+/*
+ * Zero-fills a workspace before its first use (cudaMemsetAsync on
+ * `stream`).  Every workspace passed to ds4x_index_score_topk or
+ * ds4x_sparse_attn_decode must have been zero-filled once, by this call or
+ * otherwise; each call leaves it ready for the next call on the same
+ * stream.  One workspace must not be used by two calls that may overlap on
+ * the GPU.
+ */
+int ds4x_workspace_init(void *ws, size_t ws_bytes, ds4x_stream_t stream);
+
+/*
+ * Reads the device status word at the head of a workspace (a blocking copy
+ * after synchronising `stream`) into *status_host and clears it.  It is
+ * DS4X_OK, or DS4X_EDEVICE when an attention call met an index outside
+ * [-1, n_rows) (that row was skipped), or DS4X_ETIMEOUT when a bounded wait
+ * inside the scorer gave up.  Returns DS4X_OK or DS4X_ECUDA.
+ */
+int ds4x_workspace_status(void *ws, ds4x_stream_t stream, int32_t *status_host);
+
+/*
+ * Cache writer: quantise and pack n new rows into positions [pos, pos+n).
+ * (DS4X README, "What DS4X changes": persistent history is kept as packed
+ * 583-byte KV rows and 68-byte MXFP4 indexer rows.)
+ *
+ *   kv_rows   u8 [capacity][583]  written at rows pos..pos+n-1; may be NULL
+ *   idx_rows  u8 [capacity][68]   written at rows pos..pos+n-1; may be NULL
+ *             (not both NULL; a layer without an indexer passes NULL)
+ *   kv_in     f32 [n][512]: 448 non-RoPE values then 64 RoPE values
+ *             (required when kv_rows != NULL)
+ *   idx_in    f32 [n][128] (required when idx_rows != NULL)
+ *
+ * Each 32-value indexer block and 64-value KV block gets the scale 2^e with
+ * e the least integer such that amax <= emax * 2^e (emax = 6 for E2M1, 448
+ * for E4M3; amax = 0 gives e = 0; e clamped to [-127, 127]); elements are
+ * x / 2^e rounded to nearest, ties to even, sign kept; RoPE values are
+ * rounded to FP16 (nearest even).  Output bytes are bit-exact with that
+ * rule.  Errors: DS4X_EINVAL (pointers, n < 1), DS4X_ERANGE (pos < 0 or
+ * pos + n > capacity).
+ */
+int ds4x_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t capacity, int64_t pos,
+                      const float *kv_in, const float *idx_in, int64_t n,
+                      ds4x_stream_t stream);
+
+/* Workspace bytes ds4x_index_score_topk needs for n_rows rows and k. */
+size_t ds4x_index_score_topk_workspace(int64_t n_rows, int32_t k);
+
+/*
+ * CSA indexer score + exact top-k over n_rows packed indexer rows.
+ * (DS4X README, "Optimization details": the B1 indexer reads the 68-byte
+ * rows directly; "CSA score/top-512 fusion": each scorer CTA keeps an exact
+ * local top-512 of sortable (score, index) keys and merges them, so the
+ * full score array is never materialised; float total order, lower index
+ * wins ties.)
+ *
+ *   s_t = sum_{h<64} w[h] * max(0, sum_{j<128} q[h][j] * k_t[j])
+ *
+ *   idx_rows   u8 [n_rows][68]
+ *   q_bf16     bf16 [64][128] indexer query
+ *   w          f32 [64] head weights
+ *   k          1..512
+ *   out_idx    i32 [k]: row indices, score descending then index
+ *              ascending; entries past n_rows are -1
+ *   out_score  f32 [k] or NULL: the scores (fp32 accumulation), NaN past
+ *              n_rows
+ *   ws         workspace of >= ds4x_index_score_topk_workspace(n_rows, k)
+ *              bytes, zero-filled before first use (ds4x_workspace_init)
+ *
+ * Errors: DS4X_EINVAL (pointers, n_rows < 1, k outside 1..512),
+ * DS4X_EWORKSPACE.
+ */
+int ds4x_index_score_topk(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q_bf16,
+                          const float *w, int32_t k, int32_t *out_idx, float *out_score,
+                          void *ws, size_t ws_bytes, ds4x_stream_t stream);
+
+/* Workspace bytes ds4x_sparse_attn_decode needs for k selected rows. */
+size_t ds4x_sparse_attn_decode_workspace(int32_t k);
+
+/*
+ * Sparse (indexed) decode attention over selected packed KV rows, split
+ * over row ranges with a log-sum-exp combine.  (DS4X README, "Packed cache
+ * ABI" row layout; "Nsight Systems" lists the indexed attention kernel
+ * group.)  Keys and values are the same dequantised 512-vector (448
+ * E4M3 * 2^(scale-127) values then 64 FP16 values), shared by all 64 heads:
+ *
+ *   l_hj = softmax_scale * (q_h . v_j);  p = softmax_j(l);  o_h = sum_j p_hj v_j
+ *
+ *   kv_rows        u8 [n_rows][583]
+ *   idx            i32 [k]: row indices; -1 entries are skipped; entries
+ *                  >= n_rows or < -1 are skipped and flag DS4X_EDEVICE in
+ *                  the workspace status word
+ *   k              1..512
+ *   q_bf16         bf16 [64][512]
+ *   out_bf16       bf16 [64][512] (rounded to nearest even; all-skipped
+ *                  heads give 0)
+ *   lse            f32 [64] or NULL: max_j l_hj + log(sum_j exp(l_hj - max))
+ *                  (-inf when every row was skipped)
+ *   ws             >= ds4x_sparse_attn_decode_workspace(k) bytes, zero-filled
+ *                  before first use
+ *
+ * Errors: DS4X_EINVAL (pointers, n_rows < 1, k outside 1..512),
+ * DS4X_EWORKSPACE.
+ */
+int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
+                            int32_t k, const uint16_t *q_bf16, float softmax_scale,
+                            uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
+                            ds4x_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4X_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol include/ds4x.h declares,
+and its host-side argument checks reject bad calls before any CUDA call
+(so these run without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT, golden
+
+HEADER = os.path.join(ROOT, "include", "ds4x.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_kv_sparse_csa_gb300 import build as B
+
+    if not os.path.exists(B.LIB_PATH):
+        B.build()
+    from compressed_kv_sparse_csa_gb300 import binding
+
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds4x_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_every_declared_function():
+    from compressed_kv_sparse_csa_gb300 import binding
+
+    for n in declared_functions():
+        assert n in binding._SIGNATURES, n
+
+
+def test_host_only_calls(lib):
+    assert lib.ds4x_abi_version() == 1
+    assert lib.ds4x_status_str(0) == b"ok"
+    assert b"workspace" in lib.ds4x_status_str(-3)
+    g = golden("packed_cache_abi.txt")
+    assert lib.ds4x_cache_bytes(int(g["alloc_L"])) == int(g["alloc_total"])
+    assert lib.ds4x_cache_bytes(0) == int(g["alloc_raw_rings"]) + 21 * 2 * 651 + 20 * 2 * 583
+    assert lib.ds4x_cache_bytes(-1) == -1
+    assert lib.ds4x_index_score_topk_workspace(1 << 20, 512) >= 256
+    assert lib.ds4x_sparse_attn_decode_workspace(512) >= 256 + 16 * 64 * 514 * 4
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails its host check first
+
+
+def test_append_argument_checks(lib):
+    f = lib.ds4x_cache_append
+    assert f(None, None, 10, 0, FAKE, FAKE, 1, None) == -1  # no destination
+    assert f(FAKE, None, 10, 0, None, None, 1, None) == -1  # kv_rows without kv_in
+    assert f(FAKE + 4, None, 10, 0, FAKE, None, 1, None) == -1  # misaligned
+    assert f(FAKE, FAKE, 10, 0, FAKE, FAKE, 0, None) == -1  # n < 1
+    assert f(FAKE, FAKE, 10, 8, FAKE, FAKE, 3, None) == -2  # pos + n > capacity
+    assert f(FAKE, FAKE, 10, -1, FAKE, FAKE, 1, None) == -2
+
+
+def test_score_argument_checks(lib):
+    f = lib.ds4x_index_score_topk
+    ws = lib.ds4x_index_score_topk_workspace(1000, 512)
+    assert f(None, 1000, FAKE, FAKE, 512, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 0, FAKE, FAKE, 512, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 1000, FAKE, FAKE, 0, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 1000, FAKE, FAKE, 513, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 1000, FAKE + 8, FAKE, 512, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 1000, FAKE, FAKE, 512, FAKE, None, FAKE, ws - 1, None) == -3
+
+
+def test_attention_argument_checks(lib):
+    f = lib.ds4x_sparse_attn_decode
+    ws = lib.ds4x_sparse_attn_decode_workspace(512)
+    s = ctypes.c_float(0.044)
+    assert f(FAKE, 10, None, 512, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 0, FAKE, 512, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 10, FAKE, 600, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 10, FAKE, 512, FAKE, s, FAKE, FAKE + 4, FAKE, ws, None) == -1
+    assert f(FAKE, 10, FAKE, 512, FAKE, s, FAKE, None, FAKE, 100, None) == -3
+
+
+def test_workspace_calls_reject_null(lib):
+    assert lib.ds4x_workspace_init(None, 4096, None) == -1
+    assert lib.ds4x_workspace_init(FAKE, 16, None) == -1
+    out = ctypes.c_int32(0)
+    assert lib.ds4x_workspace_status(None, None, ctypes.byref(out)) == -1
