@@ -198,6 +198,32 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
                             uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
                             ds4x_stream_t stream);
 
+/*
+ * Allocation-free form of ds4x_sparse_attn_decode, for callers that cannot
+ * allocate device memory when they decode: an engine whose device memory is
+ * partitioned once at start-up and may not grow, or a plugin hosted by a
+ * runtime that exposes no allocator, where a cudaMalloc in the middle of a
+ * step would also synchronise the device.  The pages have no counterpart to
+ * this call; it exists for those integrations only.
+ *
+ * Arguments, results and errors are those of ds4x_sparse_attn_decode without
+ * the workspace.  The split-KV partial results live in one static device
+ * array of 2,105,600 bytes inside the library, sized for the maximum k of
+ * 512 (k outside 1..512 returns DS4X_EINVAL); every GPU that loads the
+ * library holds that array until the process exits.  The call allocates
+ * nothing and calls no allocating routine.  Its first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the one array, so calls that may overlap on the GPU (different streams, or
+ * several host threads) race and must be serialised by the caller.  Nothing
+ * in the array needs to start at zero; out-of-range indices are skipped as
+ * in ds4x_sparse_attn_decode, but with no workspace there is no status word
+ * to report them.
+ */
+int ds4x_sparse_attn_decode_noalloc(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
+                                    int32_t k, const uint16_t *q_bf16, float softmax_scale,
+                                    uint16_t *out_bf16, float *lse, ds4x_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
