@@ -288,7 +288,10 @@ def main():
             B.ds4x_sparse_attn_decode(c["kv_rows"], n, c["out_idx"], K_TOP, c["q_attn"], scale, c["out"], None,
                                       ws_a, stream=stream)
 
-    launches_per_step = {"score": 2, "attn": 2}  # kernels each entry point launches (two-stage scorer)
+    # kernels each entry point launches: the fused scorer is one kernel, the
+    # two-stage scorer two; attention is split + combine
+    two_stage = os.environ.get("DS4X_SCORER") == "two_stage"
+    launches_per_step = {"score": 2 if two_stage else 1, "attn": 2}
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -415,6 +418,7 @@ def main():
                    "step_bytes": step_bytes(n),
                    "step_roofline_frac": (step_bytes(n) / (ms_step * 1e-3) / 1e9) / peak,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "scorer_path": "two_stage" if two_stage else "fused_tcgen05",
         "roofline": {"kernel": "ds4x_index_score_topk", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,

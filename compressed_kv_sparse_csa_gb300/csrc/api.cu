@@ -35,6 +35,16 @@ int check_arch() {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? DS4X_OK : DS4X_ECUDA; }
 
+// DS4X_SCORER=two_stage selects the score-then-select path (A/B and debug);
+// the default is the fused tensor-core scorer.
+bool use_two_stage() {
+  static const bool v = [] {
+    const char *e = std::getenv("DS4X_SCORER");
+    return e != nullptr && std::strcmp(e, "two_stage") == 0;
+  }();
+  return v;
+}
+
 }  // namespace
 
 extern "C" {
@@ -98,7 +108,8 @@ int ds4x_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t capacity, int
 size_t ds4x_index_score_topk_workspace(int64_t n_rows, int32_t k) {
   (void)k;
   if (n_rows < 1) n_rows = 1;
-  return score_two_stage_ws_bytes(n_rows);
+  const size_t a = score_two_stage_ws_bytes(n_rows), b = score_fused_ws_bytes();
+  return a > b ? a : b;
 }
 
 int ds4x_index_score_topk(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q_bf16,
@@ -113,7 +124,9 @@ int ds4x_index_score_topk(const uint8_t *idx_rows, int64_t n_rows, const uint16_
   if (ws_bytes < ds4x_index_score_topk_workspace(n_rows, k)) return DS4X_EWORKSPACE;
   const int a = check_arch();
   if (a != DS4X_OK) return a;
-  return from_cuda(launch_score_two_stage(idx_rows, n_rows, q_bf16, w, k, out_idx, out_score, ws, stream));
+  if (use_two_stage())
+    return from_cuda(launch_score_two_stage(idx_rows, n_rows, q_bf16, w, k, out_idx, out_score, ws, stream));
+  return from_cuda(launch_score_fused(idx_rows, n_rows, q_bf16, w, k, out_idx, out_score, ws, stream));
 }
 
 size_t ds4x_sparse_attn_decode_workspace(int32_t k) {

@@ -73,6 +73,13 @@ cudaError_t launch_score_two_stage(const uint8_t *idx_rows, int64_t n_rows,
                                    int32_t *out_idx, float *out_score, void *ws,
                                    cudaStream_t stream);
 
+// Fused tensor-core scorer with per-CTA top-512 and a last-CTA merge.
+size_t score_fused_ws_bytes();
+int score_fused_max_ctas();
+cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q,
+                               const float *w, int32_t k, int32_t *out_idx, float *out_score, void *ws,
+                               cudaStream_t stream);
+
 size_t attn_decode_ws_bytes(int32_t k);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                int32_t k, const uint16_t *q, float scale, uint16_t *out,
