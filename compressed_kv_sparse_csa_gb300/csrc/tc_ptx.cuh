@@ -99,6 +99,42 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
+// The eight K=16 steps of one 128 x 64 x 128 tile in one instruction
+// sequence: D = A[:, 0:16] B[0:16]^T, then D += A[:, 16k:16k+16] B[16k:16k+16]^T.
+// A advances 8 tensor-memory columns per step, B 256 bytes (descriptor
+// address field + 16).
+__device__ __forceinline__ void mma_f16_ta_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc0,
+                                                uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc0), "r"(idesc)
+      : "memory");
+}
+
+// acc += w * r on two fp32 lanes at once (packed f32x2 FMA).
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long w, unsigned long long r,
+                                                    unsigned long long acc) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(w), "l"(r), "l"(acc));
+  return d;
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 op this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
