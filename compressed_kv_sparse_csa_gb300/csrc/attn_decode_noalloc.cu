@@ -5,20 +5,19 @@
 // memory is carved up once at start-up and never grows, or a plugin living
 // inside a runtime that offers it no allocator and where a cudaMalloc in the
 // middle of a decode step would synchronise the whole device.  This entry
-// point needs no workspace: the split-KV partial results live in one
-// file-scope device array sized for the largest legal call (k = 512 rows),
-// which every GPU that loads the library keeps for the life of the process.
-// It launches exactly the kernels ds4x_sparse_attn_decode launches.
+// point needs no workspace: the kernel keeps its split partials in shared
+// memory, and the workspace header it writes its status to is one
+// file-scope device array, which every GPU that loads the library keeps for
+// the life of the process.  It launches exactly the kernel
+// ds4x_sparse_attn_decode launches.
 #include <atomic>
 
 #include "ds4x_internal.cuh"
 
 namespace {
 
-// Header (256 B) + 16 splits x 64 heads x (m, l, 512 outputs) floats: the
-// workspace ds4x_sparse_attn_decode needs at its maximum k of 512.
-constexpr size_t kNoAllocScratchBytes =
-    ds4x::kWsHeaderBytes + size_t(DS4X_TOPK_MAX / 32) * DS4X_ATTN_HEADS * (2 + DS4X_KV_DIM) * sizeof(float);
+// The workspace ds4x_sparse_attn_decode needs for any k: the 256-byte header.
+constexpr size_t kNoAllocScratchBytes = ds4x::kWsHeaderBytes;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
@@ -61,7 +60,6 @@ extern "C" int ds4x_sparse_attn_decode_noalloc(const uint8_t *kv_rows, int64_t n
   if (!aligned16(kv_rows) || !aligned16(idx) || !aligned16(q_bf16) || !aligned16(out_bf16) ||
       (lse != nullptr && !aligned16(lse)))
     return DS4X_EINVAL;
-  // the scratch array holds the partials of at most DS4X_TOPK_MAX rows
   if (n_rows < 1 || k < 1 || k > DS4X_TOPK_MAX) return DS4X_EINVAL;
   if (ds4x::attn_decode_ws_bytes(k) > kNoAllocScratchBytes) return DS4X_EWORKSPACE;
   int st = require_gb300();

@@ -170,7 +170,8 @@ size_t ds4x_sparse_attn_decode_workspace(int32_t k);
 
 /*
  * Sparse (indexed) decode attention over selected packed KV rows, split
- * over row ranges with a log-sum-exp combine.  (DS4X README, "Packed cache
+ * over row ranges with a log-sum-exp combine (one kernel: the splits of a
+ * head group form a thread-block cluster and combine in shared memory).  (DS4X README, "Packed cache
  * ABI" row layout; "Nsight Systems" lists the indexed attention kernel
  * group.)  Keys and values are the same dequantised 512-vector (448
  * E4M3 * 2^(scale-127) values then 64 FP16 values), shared by all 64 heads:
@@ -207,9 +208,9 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
  * this call; it exists for those integrations only.
  *
  * Arguments, results and errors are those of ds4x_sparse_attn_decode without
- * the workspace.  The split-KV partial results live in one static device
- * array of 2,105,600 bytes inside the library, sized for the maximum k of
- * 512 (k outside 1..512 returns DS4X_EINVAL); every GPU that loads the
+ * the workspace.  The workspace (its 256-byte status header; the split
+ * partials stay in shared memory) is one static device array inside the
+ * library (k outside 1..512 returns DS4X_EINVAL); every GPU that loads the
  * library holds that array until the process exits.  The call allocates
  * nothing and calls no allocating routine.  Its first call on a device looks
  * up the array's device address (cudaGetSymbolAddress, with that device
