@@ -46,6 +46,31 @@ __device__ __forceinline__ float key_score(uint64_t key) {
   return ordered_to_float(uint32_t(key >> 32));
 }
 
+// ---------------------------------------------------------------------------
+// Block-scale helpers shared by the cache writer and the scorer's query split.
+// ---------------------------------------------------------------------------
+// Least integer e with amax <= emax * 2^e, where emax = g * 2^G (0.5 <= g < 1):
+// with amax = f * 2^F, e = F - G when f <= g, else F - G + 1.
+__device__ __forceinline__ int block_exponent(float amax, float g, int G) {
+  if (amax == 0.0f) return 0;
+  int F;
+  const float f = frexpf(amax, &F);
+  const int e = F - G + (f > g ? 1 : 0);
+  return max(-127, min(127, e));
+}
+
+// 2^-e as a float, for e in [-127, 126] (every exponent a finite block can have).
+__device__ __forceinline__ float pow2_neg(int e) {
+  return __uint_as_float(uint32_t(127 - e) << 23);
+}
+
+// Two floats -> two E4M3 codes: `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Raises a kernel's dynamic shared-memory limit, once per device.
 template <typename Kernel>
 cudaError_t set_max_smem_once(Kernel *kernel, int bytes, std::atomic<uint64_t> &done_mask) {

@@ -12,21 +12,6 @@
 namespace ds4x {
 namespace {
 
-// Least integer e with amax <= emax * 2^e, where emax = g * 2^G (0.5 <= g < 1):
-// with amax = f * 2^F, e = F - G when f <= g, else F - G + 1.
-__device__ __forceinline__ int block_exponent(float amax, float g, int G) {
-  if (amax == 0.0f) return 0;
-  int F;
-  const float f = frexpf(amax, &F);
-  const int e = F - G + (f > g ? 1 : 0);
-  return max(-127, min(127, e));
-}
-
-// 2^-e as a float, for e in [-127, 126] (every exponent a finite block can have).
-__device__ __forceinline__ float pow2_neg(int e) {
-  return __uint_as_float(uint32_t(127 - e) << 23);
-}
-
 // Two floats -> one byte of two E2M1 codes: `lo` in bits 0-3, `hi` in bits 4-7.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
   uint16_t r;
@@ -35,12 +20,6 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
   return r & 0xffu;
 }
 
-// Two floats -> two E4M3 codes: `lo` in bits 0-7, `hi` in bits 8-15.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 __device__ __forceinline__ float warp_max(float v, int width) {
   for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -8,34 +8,38 @@
 //
 //  * warp 16 streams the CTA's contiguous range of 128-row tiles (8,704 bytes
 //    each) from HBM with 1-D bulk copies into a ring of shared-memory stages;
-//  * converter warpgroups 0-1 (thread = row) dequantise a tile: each byte of
-//    two E2M1 codes goes through the hardware e2m1x2 -> f16x2 converter, then
-//    one f16x2 multiply applies the block's scale relative to the row's
-//    largest block scale 2^e_ref; the 64 words go straight into a tensor-
-//    memory A slot (four-slot ring), never through shared memory;
-//  * warp 17 issues the tile's eight tcgen05.mma kind::f16 (M = 128 rows,
-//    N = 64 heads, K = 16) against the fp16 query (B, shared memory) into a
-//    tensor-memory accumulator slot (four-slot ring) and commits the tile's
-//    completion to both rings.  The issuing warp competes for issue slots
-//    with the converter and epilogue warps, so those keep their FP32-pipe
-//    work small (the epilogue's ReLU runs on the integer pipe);
+//  * converter warpgroups 0-1 (thread = row) move a tile into tensor memory as
+//    the MMA's A operand: each E2M1 code gets its own byte (code in bits 5-2,
+//    four codes per 32-bit column, 32 columns per row; a shift, a mask and a
+//    byte permute per eight codes), and the row's four UE8M0 bytes go to the
+//    row's scale-factor column (six-slot ring);
+//  * warps 17-18 (alternate tiles; a thread that waits on an mbarrier stalls
+//    until its own MMAs drain, so two issuers keep the tensor core busy)
+//    issue the tile's eight block-scaled tcgen05.mma kind::mxf8f6f4 (M = 128
+//    rows, N = 64 heads, K = 32; A = E2M1 keys with their own UE8M0 scales,
+//    B = one of the query's two E4M3 pieces with its UE8M0 scales per 32
+//    elements; both pieces accumulate into the same fp32 accumulator slot of
+//    a four-slot tensor-memory ring), so the hardware applies both sets of
+//    block scales and every row's 64 dot products come out in fp32;
 //  * epilogue warpgroups 2-3 read a row's 64 accumulators back and form
-//    s = 2^e_ref * sum_h (w_h / 2^a_h) * ReLU(acc_h) with the ReLU as a
-//    signed-integer max on the float bits and packed f32x2 FMAs, which is
-//    sum_h w_h * ReLU(q_h . k) up to fp32 rounding; each key goes into shared
-//    memory and into a fixed 8,192-bucket histogram of its score bits;
+//    s = sum_h w_h * ReLU(acc_h) (one max and one FMA per head); each key
+//    goes into shared memory and into a fixed 8,192-bucket histogram of its
+//    score bits;
 //  * after the stream one scan of the histogram locates the CTA's 512th and
 //    16th keys; one pass keeps the keys at or above the 512th key's bucket
 //    (a superset of the local top-512) and resolves the exact top-16; the
-//    CTA publishes both; the last CTA to finish sorts the CTAs' top-16
-//    sets together (a register-blocked bitonic merge of the sorted lists),
-//    fetches the supersets of any CTA whose 16th key beats the k-th key (so
-//    the result is exact for every input) and writes the outputs.
+//    CTA publishes both; the last CTA to finish merges the CTAs' top-16
+//    sets with a counting sort, fetches the supersets of any CTA whose 16th
+//    key beats the k-th key (so the result is exact for every input) and
+//    writes the outputs.
 //
-// The query is held in fp16 with a per-head power-of-two scale 2^a_h that
-// puts the head's largest |q| in [2^15, 2^16): every bf16 element within
-// 2^-32 of its head's maximum converts exactly.  Keys are exact in fp16
-// whenever a row's block exponents differ by at most 23.
+// The bf16 query q is split per head and 32-element block into E4M3 pieces
+// q = hi * 2^a + lo * 2^b, each with the block-scale rule of the cache writer
+// (a the least exponent with max|q| <= 448 * 2^a, b the same for the
+// remainder q - hi * 2^a).  The split is exact for every element within
+// 2^-14 of its block's largest magnitude (both pieces then carry four of its
+// eight significant bits); smaller elements keep their top bits.  E2M1 keys
+// times E4M3 pieces are exact products; the tensor core sums them in fp32.
 #include <cuda_fp16.h>
 
 #include "ds4x_internal.cuh"
@@ -48,33 +52,52 @@ using namespace ptx;
 
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * DS4X_IDX_ROW_BYTES;  // 8704
-constexpr int kStages = 8;
+constexpr int kStages = 10;
 constexpr int kConvWG = 2;                 // converter warpgroups: warps 0-7
 constexpr int kEpiWG = 2;                  // epilogue warpgroups: warps 8-15
 constexpr int kWGThreads = 128 * (kConvWG + kEpiWG);  // 512
 constexpr int kProducerWarp = kWGThreads / 32;        // 16
-constexpr int kMmaWarp = kProducerWarp + 1;           // 17: allocates tensor memory, issues MMAs
-constexpr int kThreads = kWGThreads + 64;             // 576
-constexpr int kSlots = 4;                  // TMEM A ring and D ring depth
-constexpr int kErefRing = 8;
+constexpr int kMmaWarp = kProducerWarp + 1;           // 17: allocates tensor memory; 17-18 issue MMAs
+constexpr int kMmaWarps = 2;                          // tile i is issued by warp kMmaWarp + i % 2
+constexpr int kThreads = kWGThreads + 32 * (1 + kMmaWarps);  // 608
+constexpr int kASlots = 6;                 // tensor-memory A ring
+constexpr int kDSlots = 4;                 // tensor-memory accumulator ring
 constexpr int kChunkTiles = 64;
 constexpr int kLocalK = DS4X_TOPK_MAX;     // 512
 constexpr int kKeysCap = kLocalK + kChunkTiles * kTileRows;  // 8704
-constexpr int kSelPerThread = 18;          // 18 * 512 >= kKeysCap and >= 256 * 16 + 512
+constexpr int kSelPerThread = 17;          // 17 * 512 >= kKeysCap and >= 256 * 16 + 512
 constexpr int kTopM = 16;
 constexpr int kPubCap = 1024;              // keys a CTA may publish (its top-16, then a superset of the rest)
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kDCol0 = 0;             // D slot j: columns [64j, 64j + 64)
-constexpr uint32_t kACol0 = 256;           // A slot j: columns [256 + 64j, 256 + 64j + 64)
-constexpr uint32_t kBqBytes = DS4X_IDX_HEADS * DS4X_IDX_DIM * 2;  // 16384
-constexpr uint32_t kBqSbo = (DS4X_IDX_DIM / 8) * 128;           // 2048: next 8 heads
-constexpr uint32_t kBqLbo = 128;                                 // next 8 K elements
-constexpr uint32_t kIdesc = idesc_f16_f32(128, DS4X_IDX_HEADS);
+constexpr int kN = DS4X_IDX_HEADS;         // 64 heads per MMA; B rows 0-63 hold the hi pieces, 64-127 the lo pieces
+constexpr uint32_t kDCol0 = 0;             // D slot j: columns [64 j, 64 j + 64)
+constexpr uint32_t kACol0 = 64 * kDSlots;  // A slot a: 32 columns from kACol0 + 32 a
+constexpr uint32_t kSfaCol0 = kACol0 + 32 * kASlots;  // SFA of A slot a: 4 columns from kSfaCol0 + 4 a
+constexpr uint32_t kSfbCol = kSfaCol0 + 4 * kASlots;  // SFB of the hi pieces: columns +0, +1
+constexpr uint32_t kSfbLoCol = kSfbCol + 4;           // SFB of the lo pieces: columns +0, +1
+constexpr uint32_t kOpBytes = 128 * DS4X_IDX_DIM;  // 16384: 128 rows x 8 K chunks of 16 bytes
+constexpr uint32_t kLbo = 128;             // next 16-element K chunk
+constexpr uint32_t kSbo = 8 * 128;         // next 8 rows
+constexpr uint32_t kIdesc = idesc_mxf8f6f4_e2m1_e4m3(kN);
 constexpr unsigned long long kTimeoutNs = 500ull * 1000 * 1000;  // a bounded wait gives up after 0.5 s
+constexpr uint32_t kWaitHintNs = 2000;     // a waiting thread may sleep in hardware up to 2 us per poll
 constexpr uint32_t kBarSel = 1;            // named barrier of the 512 warpgroup threads
+static_assert(kDSlots * 64 <= int(kACol0) && kACol0 + 32 * kASlots <= kSfaCol0 && kSfbLoCol + 4 <= uint32_t(kTmemCols),
+              "tensor-memory map");
+static_assert(kSfaCol0 % 4 == 0 && kSfbCol % 4 == 0 && kSfbLoCol % 4 == 0,
+              "scale-factor columns start on a 4-column boundary");
+static_assert(kSelPerThread * kWGThreads >= kKeysCap, "selection registers cover the key buffer");
+static_assert(kDSlots % kMmaWarps == 0, "each MMA warp owns its own accumulator slots");
+constexpr int kMaxDynSmem = 232448;         // 227 KB per CTA on sm_103
+
+// Byte offset of (row r, K element kk) in a canonical no-swizzle K-major
+// operand of 8-bit containers with 16-element chunks.
+__device__ __forceinline__ uint32_t op_offset(int r, int kk) {
+  return uint32_t(r >> 3) * kSbo + uint32_t(kk >> 4) * kLbo + uint32_t(r & 7) * 16 + uint32_t(kk & 15);
+}
 
 struct SelShared {
   unsigned long long red_min[16], red_max[16];
@@ -85,7 +108,7 @@ struct SelShared {
 };
 
 struct __align__(1024) Smem {
-  uint8_t bq[kBqBytes];                       // query, fp16, canonical no-swizzle K-major
+  uint8_t bq[kOpBytes];                       // query pieces, E4M3, canonical K-major (B)
   uint8_t stage[kStages][kTileBytes];         // raw tile ring
   unsigned long long keys[kKeysCap];          // [0, 512): carried keys; then the chunk's keys
   unsigned long long out[kLocalK];
@@ -93,11 +116,10 @@ struct __align__(1024) Smem {
   unsigned long long top16[32];
   unsigned long long b16[32];
   uint32_t hist[kHistWords];                  // fixed histogram, or the adaptive one inside select_top
-  alignas(16) float wq[DS4X_IDX_HEADS];       // w_h * 2^-a_h
-  int eref[kErefRing][kTileRows];
+  alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
+  uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
   unsigned long long full[kStages], empty[kStages];
-  unsigned long long afull[kSlots], aempty[kSlots], dfull[kSlots], dempty[kSlots];
-  unsigned long long ereff[kErefRing];
+  unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots], dempty[kDSlots];
   SelShared sel;
   int fetch[kMaxCtas];
   uint32_t tmem_base;
@@ -125,7 +147,7 @@ __device__ bool wait_bar(Smem &sm, unsigned long long *bar, uint32_t parity, WsH
   if (mbar_try_wait(b, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (mbar_try_wait_sleep(b, parity, kWaitHintNs)) return true;
     if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) return false;
     if (globaltimer() - t0 > kTimeoutNs) {
       atomicExch(&hdr->status, int32_t(DS4X_ETIMEOUT));
@@ -144,9 +166,11 @@ __device__ void drain_bar(unsigned long long *bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float scale_by_pow2(float s, int e) {
-  if (e >= -126 && e <= 127) return s * __uint_as_float(uint32_t(e + 127) << 23);
-  return ldexpf(s, e);
+// Two E4M3 codes (low byte: the first) -> their values, exactly (through f16x2).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(two_codes));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
 }
 
 // Fixed histogram bucket of a key: the top 14 bits of its ordered score bits
@@ -558,13 +582,14 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kTileRows);
     }
-    for (int j = 0; j < kSlots; ++j) {
+    for (int j = 0; j < kASlots; ++j) {
       mbar_init(smem_u32(&sm.afull[j]), kTileRows);
       mbar_init(smem_u32(&sm.aempty[j]), 1);
+    }
+    for (int j = 0; j < kDSlots; ++j) {
       mbar_init(smem_u32(&sm.dfull[j]), 1);
       mbar_init(smem_u32(&sm.dempty[j]), kTileRows);
     }
-    for (int j = 0; j < kErefRing; ++j) mbar_init(smem_u32(&sm.ereff[j]), kTileRows);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -573,28 +598,58 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
     tmem_relinquish();
   }
   if (tid < kWGThreads) {
-    // query -> fp16 B operand with a per-head power-of-two scale
-    for (int h = warp * 4; h < warp * 4 + 4; ++h) {
-      const uint2 raw = reinterpret_cast<const uint2 *>(q + h * DS4X_IDX_DIM)[lane];
-      float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                    __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
-      float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      int a = 0;
-      if (amax > 0.0f) {
-        int F;
-        frexpf(amax, &F);  // amax in [2^(F-1), 2^F)
-        a = 16 - F;        // scaled max in [2^15, 2^16)
-      }
+    // query -> two E4M3 pieces per 32-element block (B rows h and 64 + h);
+    // thread t < 256 takes head t / 4, block t % 4 (32 elements, 64 bytes)
+    if (tid < DS4X_IDX_HEADS * 4) {
+      const int h = tid >> 2, b = tid & 3;
+      const uint4 *src = reinterpret_cast<const uint4 *>(q + h * DS4X_IDX_DIM + 32 * b);
+      uint4 raw[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int kk = 4 * lane + e;
-        const __half hv = __float2half_rn(ldexpf(x[e], a));
-        const uint32_t off = (h >> 3) * kBqSbo + (kk >> 3) * kBqLbo + (h & 7) * 16 + (kk & 7) * 2;
-        *reinterpret_cast<__half *>(sm.bq + off) = hv;
+      for (int v = 0; v < 4; ++v) raw[v] = src[v];
+      float x[32];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t wv[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          x[8 * v + 2 * u] = __uint_as_float(wv[u] << 16);
+          x[8 * v + 2 * u + 1] = __uint_as_float(wv[u] & 0xffff0000u);
+        }
       }
-      if (lane == 0) sm.wq[h] = ldexpf(w[h], -a);
+      float amax = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      const int e_hi = block_exponent(amax, 0.875f, 9);  // 448 = 0.875 * 2^9
+      const float s_hi = pow2_neg(e_hi), u_hi = pow2_neg(-e_hi);
+      uint32_t hw[8];
+      float rmax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {  // elements 2j, 2j+1
+        const uint32_t c2 = cvt_e4m3x2(x[2 * j + 1] * s_hi, x[2 * j] * s_hi);
+        const float2 hv = e4m3x2_to_float2(c2);
+        x[2 * j] -= hv.x * u_hi;  // exact remainders
+        x[2 * j + 1] -= hv.y * u_hi;
+        rmax = fmaxf(rmax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+        if (j & 1) hw[j >> 1] |= c2 << 16; else hw[j >> 1] = c2;
+      }
+      const int e_lo = block_exponent(rmax, 0.875f, 9);
+      const float s_lo = pow2_neg(e_lo);
+      uint32_t lw[8];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t c2 = cvt_e4m3x2(x[2 * j + 1] * s_lo, x[2 * j] * s_lo);
+        if (j & 1) lw[j >> 1] |= c2 << 16; else lw[j >> 1] = c2;
+      }
+      // elements 32 b .. 32 b + 31 are two 16-element chunks of rows h and 64 + h
+      *reinterpret_cast<uint4 *>(sm.bq + op_offset(h, 32 * b)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(sm.bq + op_offset(h, 32 * b + 16)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+      *reinterpret_cast<uint4 *>(sm.bq + op_offset(DS4X_IDX_HEADS + h, 32 * b)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4 *>(sm.bq + op_offset(DS4X_IDX_HEADS + h, 32 * b + 16)) =
+          make_uint4(lw[4], lw[5], lw[6], lw[7]);
+      sm.sfb[h][b] = uint8_t(e_hi + 127);
+      sm.sfb[DS4X_IDX_HEADS + h][b] = uint8_t(e_lo + 127);
     }
+    for (int h = tid; h < DS4X_IDX_HEADS; h += kWGThreads) sm.wq[h] = w[h];
     for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
     for (int i = tid; i < kHistWords; i += kWGThreads) sm.hist[i] = 0u;
   }
@@ -603,6 +658,20 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
+  if (warp < 4) {
+    // query-piece scale factors: column n of a 64-row B piece reads lane
+    // n % 32 of every sub-partition, column base + n / 32, byte = K block
+    uint32_t v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint32_t *>(sm.sfb[32 * c + lane]);
+    const uint32_t lanes = uint32_t(32 * warp) << 16;
+    tc_st_x4(tmem_base + lanes + kSfbCol, v[0], v[1], 0u, 0u);
+    tc_st_x4(tmem_base + lanes + kSfbLoCol, v[2], v[3], 0u, 0u);
+    tc_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == kProducerWarp) {
     // ---- producer: bulk-copy tiles into the stage ring ---------------------
@@ -626,24 +695,27 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
         for (int i = max(0, issued - kStages); i < issued; ++i) drain_bar(&sm.full[i % kStages], (i / kStages) & 1);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---- MMA issuer ---------------------------------------------------------
+  } else if (warp >= kMmaWarp) {
+    // ---- MMA issuers: warp kMmaWarp + m takes tiles m, m + 2, ... ------------
     if (lane == 0) {
-      const uint64_t bdesc = smem_desc_noswizzle(smem_u32(sm.bq), kBqLbo, kBqSbo);
+      const uint64_t bdesc_hi = smem_desc_noswizzle(smem_u32(sm.bq), kLbo, kSbo);
+      const uint64_t bdesc_lo = smem_desc_noswizzle(smem_u32(sm.bq + op_offset(DS4X_IDX_HEADS, 0)), kLbo, kSbo);
       int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int j = i % kSlots;
-        if (!wait_bar(sm, &sm.afull[j], (i / kSlots) & 1, hdr)) break;
-        if (i >= kSlots && !wait_bar(sm, &sm.dempty[j], ((i / kSlots) - 1) & 1, hdr)) break;
+      for (int i = warp - kMmaWarp; i < n_tiles; i += kMmaWarps) {
+        const int a = i % kASlots, d = i % kDSlots;
+        if (!wait_bar(sm, &sm.afull[a], (i / kASlots) & 1, hdr)) break;
+        if (i >= kDSlots && !wait_bar(sm, &sm.dempty[d], ((i / kDSlots) - 1) & 1, hdr)) break;
         tc_fence_after();
-        mma_f16_ta_k128(tmem_base + kDCol0 + uint32_t(64 * j), tmem_base + kACol0 + uint32_t(64 * j), bdesc,
-                        kIdesc);
-        tc_commit(smem_u32(&sm.aempty[j]));
-        tc_commit(smem_u32(&sm.dfull[j]));
+        mma_mxf8f6f4_ta_k128_2b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a), bdesc_hi,
+                                bdesc_lo, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a), tmem_base + kSfbCol,
+                                tmem_base + kSfbLoCol);
+        tc_commit(smem_u32(&sm.aempty[a]));
+        tc_commit(smem_u32(&sm.dfull[d]));
         issued = i + 1;
       }
-      if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
-        for (int i = max(0, issued - kSlots); i < issued; ++i) drain_bar(&sm.dfull[i % kSlots], (i / kSlots) & 1);
+      if (*reinterpret_cast<volatile int *>(&sm.abort_flag) && issued > 0) {
+        const int i = issued - 1;  // this thread's last commit covers all of its MMAs
+        drain_bar(&sm.dfull[i % kDSlots], (i / kDSlots) & 1);
       }
     }
   } else if (warp < kProducerWarp) {
@@ -656,87 +728,61 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
     for (int c0 = 0; c0 < n_tiles; c0 += kChunkTiles) {
       const int c1 = min(n_tiles, c0 + kChunkTiles);
       for (int i = c0 + role_wg; i < c1; i += n_role_wg) {
-        const int j = i % kSlots;
-        const int er = i % kErefRing;
         if (is_conv) {
-          // ---- convert: raw row -> fp16 A slot ------------------------------
-          const int s = i % kStages;
-          wait_bar(sm, &sm.full[s], (i / kStages) & 1, hdr);
+          // ---- raw row -> A slot (one code per byte) + scale-factor word -----
+          const int st = i % kStages, a = i % kASlots;
+          wait_bar(sm, &sm.full[st], (i / kStages) & 1, hdr);
           uint32_t wd[17];
-          const uint32_t *rp = reinterpret_cast<const uint32_t *>(sm.stage[s] + r * DS4X_IDX_ROW_BYTES);
+          const uint32_t *rp = reinterpret_cast<const uint32_t *>(sm.stage[st] + r * DS4X_IDX_ROW_BYTES);
 #pragma unroll
           for (int t = 0; t < 17; ++t) wd[t] = rp[t];
-          mbar_arrive(smem_u32(&sm.empty[s]));
-          int eb[4], eref = -1000;
+          mbar_arrive(smem_u32(&sm.empty[st]));
+          if (i >= kASlots) wait_bar(sm, &sm.aempty[a], ((i / kASlots) - 1) & 1, hdr);
+          // word t holds codes 8t..8t+7 (even code in the low nibble); column c
+          // of the slot takes codes 4c..4c+3, one per byte, shifted to bits 5-2
+          uint32_t av[32];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            eb[b] = int((wd[16] >> (8 * b)) & 0xffu) - 127;
-            eref = max(eref, eb[b]);
+          for (int t = 0; t < 16; ++t) {
+            const uint32_t ev = (wd[t] << 2) & 0x3c3c3c3cu;  // codes 8t, 8t+2, 8t+4, 8t+6
+            const uint32_t od = (wd[t] >> 2) & 0x3c3c3c3cu;  // codes 8t+1, 8t+3, 8t+5, 8t+7
+            av[2 * t] = __byte_perm(ev, od, 0x5140);
+            av[2 * t + 1] = __byte_perm(ev, od, 0x7362);
           }
-          uint32_t f2[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int d = max(eb[b] - eref, -24);
-            const uint32_t h = d >= -14 ? uint32_t(15 + d) << 10 : (1u << (d + 24));  // fp16 2^d
-            f2[b] = h | (h << 16);
-          }
-          if (i >= kSlots) wait_bar(sm, &sm.aempty[j], ((i / kSlots) - 1) & 1, hdr);
-          sm.eref[er][r] = eref;
-          mbar_arrive(smem_u32(&sm.ereff[er]));
-          const uint32_t a_t = tmem_base + lane_base + kACol0 + uint32_t(64 * j);
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t a[32];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const uint32_t word = wd[half * 8 + t];
-              const uint32_t f = f2[(half * 8 + t) >> 2];
-              a[4 * t + 0] = hmul2(e2m1x2_to_f16x2(word), f);
-              a[4 * t + 1] = hmul2(e2m1x2_to_f16x2(word >> 8), f);
-              a[4 * t + 2] = hmul2(e2m1x2_to_f16x2(word >> 16), f);
-              a[4 * t + 3] = hmul2(e2m1x2_to_f16x2(word >> 24), f);
-            }
-            tc_st_x32(a_t + uint32_t(half * 32), a);
-          }
+          tc_st_x32(tmem_base + lane_base + kACol0 + uint32_t(32 * a), av);
+          // row r's scales: lane r, column kSfaCol0 + 4 a + r / 32
+          tc_st_x1(tmem_base + lane_base + kSfaCol0 + uint32_t(4 * a + (warp & 3)), wd[16]);
           tc_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&sm.afull[j]));
+          mbar_arrive(smem_u32(&sm.afull[a]));
         } else {
           // ---- epilogue: accumulators -> score -> key --------------------------
-          bool ok = wait_bar(sm, &sm.dfull[j], (i / kSlots) & 1, hdr);
-          ok = wait_bar(sm, &sm.ereff[er], (i / kErefRing) & 1, hdr) && ok;
-          const int eref = sm.eref[er][r];
+          const int d = i % kDSlots;
+          const bool ok = wait_bar(sm, &sm.dfull[d], (i / kDSlots) & 1, hdr);
           tc_fence_after();
-          const uint32_t d_t = tmem_base + lane_base + kDCol0 + uint32_t(64 * j);
-          uint32_t d0[32], d1[32];
-          tc_ld_x32(d_t, d0);
-          tc_ld_x32(d_t + 32u, d1);
-          tc_wait_ld();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.dempty[j]));
-          // ReLU(x) as max(int bits, 0): a negative float (or -0) has negative
-          // int bits, a positive one keeps its bits
-          unsigned long long acc2[4] = {0ull, 0ull, 0ull, 0ull};
-          const ulonglong2 *wq2 = reinterpret_cast<const ulonglong2 *>(sm.wq);
+          const uint32_t d_t = tmem_base + lane_base + kDCol0 + uint32_t(64 * d);
+          const float4 *w4 = reinterpret_cast<const float4 *>(sm.wq);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int h4 = 0; h4 < 16; ++h4) {
-            const ulonglong2 wv = wq2[h4];
-            const uint32_t *src = h4 < 8 ? d0 + 4 * h4 : d1 + 4 * (h4 - 8);
-            const unsigned long long r01 = uint64_t(uint32_t(max(int(src[0]), 0))) |
-                                           (uint64_t(uint32_t(max(int(src[1]), 0))) << 32);
-            const unsigned long long r23 = uint64_t(uint32_t(max(int(src[2]), 0))) |
-                                           (uint64_t(uint32_t(max(int(src[3]), 0))) << 32);
-            acc2[(2 * h4) & 3] = ffma2(wv.x, r01, acc2[(2 * h4) & 3]);
-            acc2[(2 * h4 + 1) & 3] = ffma2(wv.y, r23, acc2[(2 * h4 + 1) & 3]);
-          }
-          float part[8];
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v0[16], v1[16];
+            tc_ld_x16(d_t + uint32_t(32 * half), v0);
+            tc_ld_x16(d_t + uint32_t(32 * half + 16), v1);
+            tc_wait_ld();
+            if (half == 1) {
+              tc_fence_before();
+              mbar_arrive(smem_u32(&sm.dempty[d]));
+            }
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            part[2 * p] = __uint_as_float(uint32_t(acc2[p]));
-            part[2 * p + 1] = __uint_as_float(uint32_t(acc2[p] >> 32));
+            for (int g = 0; g < 8; ++g) {  // heads 32 half + 4 g .. + 3
+              const float4 wv = w4[8 * half + g];
+              const uint32_t *v = g < 4 ? v0 + 4 * g : v1 + 4 * (g - 4);
+              acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), acc[0]);
+              acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), acc[1]);
+              acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), acc[2]);
+              acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), acc[3]);
+            }
           }
-          const float sum = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-          const float s_row = scale_by_pow2(sum, eref);
+          const float s_row = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           const int64_t row = (tile_begin + i) * kTileRows + r;
           unsigned long long key = 0ull;
           if (ok && row < n_rows) {
@@ -989,6 +1035,7 @@ int score_fused_max_ctas() { return kMaxCtas; }
 cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q, const float *w,
                                int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
+  static_assert(sizeof(Smem) + 1024 <= size_t(kMaxDynSmem), "shared memory budget");
   const int smem_bytes = int(sizeof(Smem)) + 1024;
   cudaError_t e = set_max_smem_once(score_fused_kernel, smem_bytes, smem_set);
   if (e != cudaSuccess) return e;

@@ -1,6 +1,7 @@
 // Thin inline-PTX wrappers for the sm_103a features the fused scorer uses:
 // mbarriers, 1-D bulk (TMA) copies, tensor memory (tcgen05.alloc/ld/st),
-// tcgen05.mma with the A operand in tensor memory, and named barriers.
+// block-scaled tcgen05.mma with the A operand in tensor memory, and named
+// barriers.
 #pragma once
 
 #include <stdint.h>
@@ -33,6 +34,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may sleep in hardware up to `hint_ns`
+// (returning early when the phase completes) instead of re-polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -76,63 +89,61 @@ __device__ __forceinline__ void tc_st_x32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ void tc_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, one CTA.  `accumulate` false
-// overwrites D.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
+// Instruction descriptor, kind::mxf8f6f4 with block scaling (UE8M0 scale
+// factors, one per 32 K-elements): A type E2M1 (5), B type E4M3 (0), both
+// K-major, fp32 D, M = 128; the scale-factor byte ids of A (bits 29-30) and
+// B (bits 4-5) are OR-ed in per K step.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e2m1_e4m3(uint32_t N) {
+  return (5u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) | (1u << 27);
 }
-// The eight K=16 steps of one 128 x 64 x 128 tile in one instruction
-// sequence: D = A[:, 0:16] B[0:16]^T, then D += A[:, 16k:16k+16] B[16k:16k+16]^T.
-// A advances 8 tensor-memory columns per step, B 256 bytes (descriptor
-// address field + 16).
-__device__ __forceinline__ void mma_f16_ta_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc0,
-                                                uint32_t idesc) {
+
+// One 128-row tile against the whole 128-element K extent and two B operands
+// (N = 64 each) summed into one accumulator: K step s (32 elements) issues
+// D (+)= (A_s * SFA_s)(B1_s * SFB1_s)^T and D += (A_s * SFA_s)(B2_s * SFB2_s)^T,
+// block-scaled.  A is in tensor memory (one E2M1 code per byte, in bits 5-2;
+// 8 columns per step), B1 and B2 in shared memory (descriptors + 16 = 256
+// bytes per step); step s reads byte s of every scale-factor word (ids s).
+// The first MMA overwrites D.  Scale-factor columns start on 4-column
+// boundaries.
+__device__ __forceinline__ void mma_mxf8f6f4_ta_k128_2b(uint32_t d_tmem, uint32_t a_tmem, uint64_t b1_desc0,
+                                                        uint64_t b2_desc0, uint32_t idesc, uint32_t sfa_tmem,
+                                                        uint32_t sfb1_tmem, uint32_t sfb2_tmem) {
   asm volatile(
-      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
-      "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
-      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc0), "r"(idesc)
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 a, id;\n\t.reg .b64 b1, b2;\n\t"
+      "setp.ne.b32 pf, %4, %4;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %4, [%5], [%6], pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %3, %4, [%5], [%7], pt;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.s64 b1, %2, 16;\n\tadd.s64 b2, %3, 16;\n\tor.b32 id, %4, 0x20000010;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b1, id, [%5], [%6], pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b2, id, [%5], [%7], pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b1, b1, 16;\n\tadd.s64 b2, b2, 16;\n\tor.b32 id, %4, 0x40000020;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b1, id, [%5], [%6], pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b2, id, [%5], [%7], pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b1, b1, 16;\n\tadd.s64 b2, b2, 16;\n\tor.b32 id, %4, 0x60000030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b1, id, [%5], [%6], pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b2, id, [%5], [%7], pt;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b1_desc0), "l"(b2_desc0), "r"(idesc), "r"(sfa_tmem), "r"(sfb1_tmem),
+        "r"(sfb2_tmem)
       : "memory");
 }
 
-// acc += w * r on two fp32 lanes at once (packed f32x2 FMA).
-__device__ __forceinline__ unsigned long long ffma2(unsigned long long w, unsigned long long r,
-                                                    unsigned long long acc) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(w), "l"(r), "l"(acc));
-  return d;
+// tcgen05.st of one / four 32-bit columns (32 lanes x 32 bits each).
+__device__ __forceinline__ void tc_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tc_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3)
+               : "memory");
 }
 
 // Arrive (once) on an mbarrier when every tcgen05 op this thread issued so far completes.
@@ -149,33 +160,12 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46);
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Two E2M1 codes (one byte, low nibble first) -> f16x2 (low half = low nibble).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.u8.u16 t, h;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(byte_in_low_bits));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
 }
 
 }  // namespace ptx
