@@ -36,6 +36,13 @@ _SIGNATURES = {
     "ds4x_sparse_attn_decode_workspace": (_c_size, [_c_i32]),
     "ds4x_sparse_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p, _c_size, _c_p]),
     "ds4x_sparse_attn_decode_noalloc": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p]),
+    "ds4x_index_score_topk_batched_workspace": (_c_size, [_c_i32, _c_i32]),
+    "ds4x_index_score_topk_batched": (ctypes.c_int, [_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size,
+                                                      _c_p]),
+    "ds4x_sparse_attn_decode_batched": (ctypes.c_int, [_c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p,
+                                                        _c_size, _c_p]),
+    "ds4x_sparse_attn_prefill": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p,
+                                                 _c_size, _c_p]),
 }
 
 
@@ -175,3 +182,53 @@ def ds4x_sparse_attn_decode_noalloc(kv_rows, n_rows, idx, k, q_bf16, softmax_sca
     _check(lse, torch.float32, "lse", numel=64, allow_none=True)
     _call("ds4x_sparse_attn_decode_noalloc", _ptr(kv_rows), int(n_rows), _ptr(idx), int(k), _ptr(q_bf16),
           float(softmax_scale), _ptr(out_bf16), _ptr(lse), _stream(stream))
+
+
+def ds4x_index_score_topk_batched_workspace(n_sess: int, k: int) -> int:
+    return lib().ds4x_index_score_topk_batched_workspace(int(n_sess), int(k))
+
+
+def ds4x_index_score_topk_batched(idx_row_ptrs, n_rows, q_bf16, w, k, out_idx, out_score, ws, stream=None):
+    """Score + exact top-k for a batch of sessions: idx_row_ptrs int64 [S]
+    holds each session's device row pointer, n_rows int64 [S] its length;
+    q_bf16 [S, 64, 128], w [S, 64], out_idx int32 [S, k]."""
+    _check(idx_row_ptrs, torch.int64, "idx_row_ptrs")
+    S = idx_row_ptrs.numel()
+    _check(n_rows, torch.int64, "n_rows", numel=S)
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=S * 64 * 128)
+    _check(w, torch.float32, "w", numel=S * 64)
+    _check(out_idx, torch.int32, "out_idx", numel=S * int(k))
+    _check(out_score, torch.float32, "out_score", numel=S * int(k), allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_index_score_topk_batched", _ptr(idx_row_ptrs), _ptr(n_rows), S, _ptr(q_bf16), _ptr(w), int(k),
+          _ptr(out_idx), _ptr(out_score), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_sparse_attn_decode_batched(kv_row_ptrs, n_rows, idx, k, q_bf16, softmax_scale, out_bf16, lse, ws,
+                                    stream=None):
+    """Decode attention for a batch of sessions: kv_row_ptrs int64 [S] device
+    row pointers, n_rows int64 [S], idx int32 [S, k], q_bf16 [S, 64, 512]."""
+    _check(kv_row_ptrs, torch.int64, "kv_row_ptrs")
+    S = kv_row_ptrs.numel()
+    _check(n_rows, torch.int64, "n_rows", numel=S)
+    _check(idx, torch.int32, "idx", numel=S * int(k))
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=S * 64 * 512)
+    _check(out_bf16, torch.bfloat16, "out_bf16", numel=S * 64 * 512)
+    _check(lse, torch.float32, "lse", numel=S * 64, allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_sparse_attn_decode_batched", _ptr(kv_row_ptrs), _ptr(n_rows), S, _ptr(idx), int(k), _ptr(q_bf16),
+          float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_sparse_attn_prefill(kv_rows, n_rows, idx, n_queries, k, q_bf16, softmax_scale, out_bf16, lse, ws,
+                             stream=None):
+    """Per-query sparse attention of q_bf16 [T, 64, 512] over each query's k
+    rows idx [T, k] of one cache."""
+    _check(kv_rows, torch.uint8, "kv_rows", numel=int(n_rows) * 583)
+    _check(idx, torch.int32, "idx", numel=int(n_queries) * int(k))
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=int(n_queries) * 64 * 512)
+    _check(out_bf16, torch.bfloat16, "out_bf16", numel=int(n_queries) * 64 * 512)
+    _check(lse, torch.float32, "lse", numel=int(n_queries) * 64, allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_sparse_attn_prefill", _ptr(kv_rows), int(n_rows), _ptr(idx), int(n_queries), int(k), _ptr(q_bf16),
+          float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))

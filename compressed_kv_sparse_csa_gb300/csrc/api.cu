@@ -151,4 +151,86 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
                                       ws, stream));
 }
 
+size_t ds4x_index_score_topk_batched_workspace(int32_t n_sess, int32_t k) {
+  (void)n_sess;
+  (void)k;
+  return score_fused_ws_bytes();
+}
+
+int ds4x_index_score_topk_batched(const uint8_t *const *idx_rows, const int64_t *n_rows, int32_t n_sess,
+                                  const uint16_t *q_bf16, const float *w, int32_t k, int32_t *out_idx,
+                                  float *out_score, void *ws, size_t ws_bytes, ds4x_stream_t stream) {
+  if (idx_rows == nullptr || n_rows == nullptr || q_bf16 == nullptr || w == nullptr || out_idx == nullptr ||
+      ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(idx_rows) || !aligned16(n_rows) || !aligned16(q_bf16) || !aligned16(w) || !aligned16(out_idx) ||
+      !aligned16(ws) || (out_score != nullptr && !aligned16(out_score)))
+    return DS4X_EINVAL;
+  if (n_sess < 1 || n_sess > DS4X_MAX_SESSIONS || k < 1 || k > DS4X_TOPK_MAX) return DS4X_EINVAL;
+  if (ws_bytes < ds4x_index_score_topk_batched_workspace(n_sess, k)) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  ScoreBatch sb{};
+  sb.rows_arr = idx_rows;
+  sb.n_arr = n_rows;
+  sb.n_sess = n_sess;
+  sb.q = q_bf16;
+  sb.w = w;
+  sb.k = k;
+  sb.out_idx = out_idx;
+  sb.out_score = out_score;
+  return from_cuda(launch_score_batch(sb, 0, ws, stream));
+}
+
+int ds4x_sparse_attn_decode_batched(const uint8_t *const *kv_rows, const int64_t *n_rows, int32_t n_sess,
+                                    const int32_t *idx, int32_t k, const uint16_t *q_bf16, float softmax_scale,
+                                    uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
+                                    ds4x_stream_t stream) {
+  if (kv_rows == nullptr || n_rows == nullptr || idx == nullptr || q_bf16 == nullptr || out_bf16 == nullptr ||
+      ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(kv_rows) || !aligned16(n_rows) || !aligned16(idx) || !aligned16(q_bf16) || !aligned16(out_bf16) ||
+      !aligned16(ws) || (lse != nullptr && !aligned16(lse)))
+    return DS4X_EINVAL;
+  if (n_sess < 1 || n_sess > DS4X_MAX_SESSIONS || k < 1 || k > DS4X_TOPK_MAX) return DS4X_EINVAL;
+  if (ws_bytes < ds4x_sparse_attn_decode_workspace(k)) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  AttnBatch ab{};
+  ab.kv_arr = kv_rows;
+  ab.n_arr = n_rows;
+  ab.idx = idx;
+  ab.k = k;
+  ab.scale = softmax_scale;
+  ab.q = q_bf16;
+  ab.out = out_bf16;
+  ab.lse = lse;
+  return from_cuda(launch_attn_batch(ab, n_sess, ws, stream));
+}
+
+int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
+                             int32_t k, const uint16_t *q_bf16, float softmax_scale, uint16_t *out_bf16,
+                             float *lse, void *ws, size_t ws_bytes, ds4x_stream_t stream) {
+  if (kv_rows == nullptr || idx == nullptr || q_bf16 == nullptr || out_bf16 == nullptr || ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(kv_rows) || !aligned16(idx) || !aligned16(q_bf16) || !aligned16(out_bf16) || !aligned16(ws) ||
+      (lse != nullptr && !aligned16(lse)))
+    return DS4X_EINVAL;
+  if (n_rows < 1 || n_queries < 1 || n_queries > DS4X_PREFILL_MAX_QUERIES || k < 1 || k > DS4X_TOPK_MAX)
+    return DS4X_EINVAL;
+  if (ws_bytes < ds4x_sparse_attn_decode_workspace(k)) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  AttnBatch ab{};
+  ab.kv = kv_rows;
+  ab.n_rows = n_rows;
+  ab.idx = idx;
+  ab.k = k;
+  ab.scale = softmax_scale;
+  ab.q = q_bf16;
+  ab.out = out_bf16;
+  ab.lse = lse;
+  return from_cuda(launch_attn_batch(ab, n_queries, ws, stream));
+}
+
 }  // extern "C"

@@ -98,9 +98,17 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
 }
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
-attn_decode_kernel(const uint8_t *__restrict__ kv, int64_t n_rows, const int32_t *__restrict__ idx,
-                   int k, const uint16_t *__restrict__ q, float scale, uint16_t *__restrict__ out,
-                   float *__restrict__ lse, WsHeader *hdr) {
+attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
+  // batch item blockIdx.z: its cache, selected rows, query and output
+  const int bz = blockIdx.z;
+  const uint8_t *__restrict__ kv = ab.kv_arr != nullptr ? ab.kv_arr[bz] : ab.kv;
+  const int64_t n_rows = ab.n_arr != nullptr ? ab.n_arr[bz] : ab.n_rows;
+  const int k = ab.k;
+  const float scale = ab.scale;
+  const int32_t *__restrict__ idx = ab.idx + size_t(bz) * k;
+  const uint16_t *__restrict__ q = ab.q + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
+  uint16_t *__restrict__ out = ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
+  float *__restrict__ lse = ab.lse != nullptr ? ab.lse + size_t(bz) * DS4X_ATTN_HEADS : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char *Kh = smem;                                                // [64][1056]: raw, then fp16
   float *Qf = reinterpret_cast<float *>(smem + kKhBytes);                 // [4][512]
@@ -351,15 +359,28 @@ attn_decode_kernel(const uint8_t *__restrict__ kv, int64_t n_rows, const int32_t
 
 size_t attn_decode_ws_bytes(int32_t) { return kWsHeaderBytes; }
 
-cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
-                               int32_t k, const uint16_t *q, float scale, uint16_t *out,
-                               float *lse, void *ws, cudaStream_t stream) {
+cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = set_max_smem_once(attn_decode_kernel, int(kSmemBytes), smem_set);
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<<<dim3(kCluster, kGroups), kThreads, kSmemBytes, stream>>>(
-      kv_rows, n_rows, idx, k, q, scale, out, lse, static_cast<WsHeader *>(ws));
+  attn_decode_kernel<<<dim3(kCluster, kGroups, batch), kThreads, kSmemBytes, stream>>>(ab,
+                                                                                      static_cast<WsHeader *>(ws));
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
+                               int32_t k, const uint16_t *q, float scale, uint16_t *out,
+                               float *lse, void *ws, cudaStream_t stream) {
+  AttnBatch ab{};
+  ab.kv = kv_rows;
+  ab.n_rows = n_rows;
+  ab.idx = idx;
+  ab.k = k;
+  ab.q = q;
+  ab.scale = scale;
+  ab.out = out;
+  ab.lse = lse;
+  return launch_attn_batch(ab, 1, ws, stream);
 }
 
 }  // namespace ds4x

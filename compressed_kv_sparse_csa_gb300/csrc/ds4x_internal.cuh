@@ -98,13 +98,47 @@ cudaError_t launch_score_two_stage(const uint8_t *idx_rows, int64_t n_rows,
                                    int32_t *out_idx, float *out_score, void *ws,
                                    cudaStream_t stream);
 
-// Fused tensor-core scorer with per-CTA top-512 and a last-CTA merge.
+// Fused tensor-core scorer with per-CTA top-512 and a last-CTA merge, over
+// one session (rows / n_rows) or a batch (device arrays rows_arr / n_arr of
+// n_sess sessions; session s reads q + s * 64 * 128, w + s * 64 and writes
+// out_idx + s k, out_score + s k).
+struct ScoreBatch {
+  const uint8_t *rows;
+  int64_t n_rows;
+  const uint8_t *const *rows_arr;
+  const int64_t *n_arr;
+  int32_t n_sess;
+  const uint16_t *q;
+  const float *w;
+  int32_t k;
+  int32_t *out_idx;
+  float *out_score;
+};
+// tiles_hint: the one session's tile count, or 0 for a batch (all SMs).
+cudaError_t launch_score_batch(const ScoreBatch &sb, int64_t tiles_hint, void *ws, cudaStream_t stream);
 size_t score_fused_ws_bytes();
 int score_fused_max_ctas();
 cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q,
                                const float *w, int32_t k, int32_t *out_idx, float *out_score, void *ws,
                                cudaStream_t stream);
 
+// Sparse attention over a batch of (cache, selected rows, query) items; item
+// b reads kv_arr[b] / n_arr[b] when those device arrays are given, else the
+// one shared cache, and idx + b k, q + b * 64 * 512, out + b * 64 * 512,
+// lse + b * 64.
+struct AttnBatch {
+  const uint8_t *kv;
+  int64_t n_rows;
+  const uint8_t *const *kv_arr;
+  const int64_t *n_arr;
+  const int32_t *idx;
+  int32_t k;
+  float scale;
+  const uint16_t *q;
+  uint16_t *out;
+  float *lse;
+};
+cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
 size_t attn_decode_ws_bytes(int32_t k);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                int32_t k, const uint16_t *q, float scale, uint16_t *out,

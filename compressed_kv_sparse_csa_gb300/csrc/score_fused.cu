@@ -71,6 +71,7 @@ constexpr int kPubCap = 1024;              // keys a CTA may publish (its top-16
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
+constexpr int kMaxSess = DS4X_MAX_SESSIONS;   // sessions one batched call may score
 constexpr int kTmemCols = 512;
 constexpr int kN = DS4X_IDX_HEADS;         // 64 heads per MMA; B rows 0-63 hold the hi pieces, 64-127 the lo pieces
 constexpr uint32_t kDCol0 = 0;             // D slot j: columns [64 j, 64 j + 64)
@@ -129,6 +130,7 @@ struct __align__(1024) Smem {
 
 struct FusedWs {
   WsHeader hdr;
+  unsigned int tickets[kMaxSess];               // per session: CTAs done (self-resetting)
   unsigned long long lists[kMaxCtas][kPubCap];  // per CTA: its top-16 (descending), then the rest
   int cnt[kMaxCtas];                            // entries in the CTA's list
   unsigned long long th16[kMaxCtas];            // CTA's 16th largest key (0: the list is all it has)
@@ -562,17 +564,52 @@ __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint16_t *__restrict__ q,
-                   const float *__restrict__ w, int k, int32_t *__restrict__ out_idx,
-                   float *__restrict__ out_score, FusedWs *__restrict__ ws) {
+score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int G = gridDim.x;
+  // ---- this CTA's session and its tile range ------------------------------
+  // One session: every CTA of the grid.  A batch: the CTAs are split across
+  // the sessions in proportion to their tile counts, at least one each, by
+  // the same arithmetic in every CTA; CTAs past the split have no work.
+  int sess = 0, cta0 = 0, Gs = gridDim.x;
+  const uint8_t *rows = sb.rows;
+  int64_t n_rows = sb.n_rows;
+  if (sb.rows_arr != nullptr) {
+    int64_t total = 0;
+    for (int s = 0; s < sb.n_sess; ++s) {
+      const int64_t nr = sb.n_arr[s];
+      total += nr > 0 ? (nr + kTileRows - 1) / kTileRows : 1;
+    }
+    const int64_t spare = int64_t(gridDim.x) - sb.n_sess;
+    int prefix = 0;
+    bool found = false;
+    for (int s = 0; s < sb.n_sess; ++s) {
+      const int64_t nr = sb.n_arr[s];
+      const int64_t t = nr > 0 ? (nr + kTileRows - 1) / kTileRows : 1;
+      const int64_t share = 1 + spare * t / total;
+      const int g = int(share < t ? share : t);
+      if (!found && int(blockIdx.x) < prefix + g) {
+        sess = s;
+        cta0 = prefix;
+        Gs = g;
+        found = true;
+      }
+      prefix += g;
+    }
+    if (!found) return;  // uniform across the CTA, before any barrier or allocation
+    rows = sb.rows_arr[sess];
+    n_rows = sb.n_arr[sess] > 0 ? sb.n_arr[sess] : 0;
+  }
+  const uint16_t *__restrict__ q = sb.q + size_t(sess) * DS4X_IDX_HEADS * DS4X_IDX_DIM;
+  const float *__restrict__ w = sb.w + size_t(sess) * DS4X_IDX_HEADS;
+  const int k = sb.k;
+  int32_t *__restrict__ out_idx = sb.out_idx + size_t(sess) * k;
+  float *__restrict__ out_score = sb.out_score != nullptr ? sb.out_score + size_t(sess) * k : nullptr;
   const int64_t n_tiles_total = (n_rows + kTileRows - 1) / kTileRows;
-  const int64_t tile_begin = n_tiles_total * blockIdx.x / G;
-  const int64_t tile_end = n_tiles_total * (blockIdx.x + 1) / G;
+  const int64_t tile_begin = n_tiles_total * (blockIdx.x - cta0) / Gs;
+  const int64_t tile_end = n_tiles_total * (blockIdx.x - cta0 + 1) / Gs;
   const int n_tiles = int(tile_end - tile_begin);
   WsHeader *hdr = &ws->hdr;
 
@@ -922,8 +959,8 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
     __threadfence();
     bar512();
     if (tid == 0) {
-      const unsigned int ticket = atomicAdd(&hdr->ticket, 1u);
-      sm.is_last = (ticket == unsigned(G - 1));
+      const unsigned int ticket = atomicAdd(&ws->tickets[sess], 1u);
+      sm.is_last = (ticket == unsigned(Gs - 1));
     }
     bar512();
 
@@ -937,16 +974,16 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int i = tid + q * kWGThreads;
-          cand[q] = i < G * kTopM ? ld_cg(&ws->lists[i / kTopM][i % kTopM]) : 0ull;
+          cand[q] = i < Gs * kTopM ? ld_cg(&ws->lists[cta0 + i / kTopM][i % kTopM]) : 0ull;
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) sm.keys[tid + q * kWGThreads] = cand[q];
       }
       bar512();
-      int sel_n = merge_topk_sorted(sm.keys, G * kTopM, kk, sm.out, sm.hist,
+      int sel_n = merge_topk_sorted(sm.keys, Gs * kTopM, kk, sm.out, sm.hist,
                                     reinterpret_cast<uint32_t *>(sm.stage[0]), sm.sel, tid);
       bool sorted_ok = sel_n >= 0;
-      if (!sorted_ok) sel_n = select_top(sm.keys, G * kTopM, kk, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+      if (!sorted_ok) sel_n = select_top(sm.keys, Gs * kTopM, kk, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
       unsigned long long cut = 0ull;
       if (sel_n == kk) {
         if (sorted_ok) {
@@ -962,15 +999,15 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
       bar512();
       if (tid == 0) sm.sel.list_cnt = 0;
       bar512();
-      for (int c0 = 0; c0 < G; c0 += kWGThreads) {
+      for (int c0 = 0; c0 < Gs; c0 += kWGThreads) {
         const int cc = c0 + tid;
-        const unsigned long long t16 = cc < G ? ld_cg(&ws->th16[cc]) : 0ull;
+        const unsigned long long t16 = cc < Gs ? ld_cg(&ws->th16[cta0 + cc]) : 0ull;
         const bool f = t16 != 0ull && t16 > cut;
         const int p = warp_append(&sm.sel.list_cnt, f);
-        if (f) sm.fetch[p] = cc;
+        if (f) sm.fetch[p] = cta0 + cc;
       }
       bar512();
-      const int n_fetch = min(sm.sel.list_cnt, G);
+      const int n_fetch = min(sm.sel.list_cnt, Gs);
       if (n_fetch == 0 && sorted_ok) {
         for (int e = tid; e < kk; e += kWGThreads) {
           if (e < sel_n) {
@@ -1014,7 +1051,7 @@ score_fused_kernel(const uint8_t *__restrict__ rows, int64_t n_rows, const uint1
           }
         }
       }
-      if (tid == 0) hdr->ticket = 0u;  // ready for the next call on this workspace
+      if (tid == 0) ws->tickets[sess] = 0u;  // ready for the next call on this workspace
     }
   }
 
@@ -1032,8 +1069,7 @@ size_t score_fused_ws_bytes() { return sizeof(FusedWs); }
 
 int score_fused_max_ctas() { return kMaxCtas; }
 
-cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q, const float *w,
-                               int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream) {
+cudaError_t launch_score_batch(const ScoreBatch &sb, int64_t tiles_hint, void *ws, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   static_assert(sizeof(Smem) + 1024 <= size_t(kMaxDynSmem), "shared memory budget");
   const int smem_bytes = int(sizeof(Smem)) + 1024;
@@ -1042,12 +1078,26 @@ cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const ui
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t tiles = (n_rows + kTileRows - 1) / kTileRows;
   const int cap = sms < kMaxCtas ? sms : kMaxCtas;
-  const int grid = tiles < cap ? int(tiles) : cap;
-  score_fused_kernel<<<grid, kThreads, smem_bytes, stream>>>(idx_rows, n_rows, q, w, k, out_idx, out_score,
-                                                             static_cast<FusedWs *>(ws));
+  // one session: no more CTAs than tiles; a batch: every SM (the kernel splits them)
+  const int grid = (tiles_hint > 0 && tiles_hint < cap) ? int(tiles_hint) : cap;
+  if (sb.rows_arr != nullptr && grid < sb.n_sess) return cudaErrorInvalidConfiguration;
+  score_fused_kernel<<<grid, kThreads, smem_bytes, stream>>>(sb, static_cast<FusedWs *>(ws));
   return cudaGetLastError();
+}
+
+cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q, const float *w,
+                               int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream) {
+  ScoreBatch sb{};
+  sb.rows = idx_rows;
+  sb.n_rows = n_rows;
+  sb.n_sess = 1;
+  sb.q = q;
+  sb.w = w;
+  sb.k = k;
+  sb.out_idx = out_idx;
+  sb.out_score = out_score;
+  return launch_score_batch(sb, (n_rows + kTileRows - 1) / kTileRows, ws, stream);
 }
 
 }  // namespace ds4x

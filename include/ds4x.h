@@ -63,6 +63,8 @@ typedef struct CUstream_st *ds4x_stream_t;
 #define DS4X_IDX_HEADS 64
 #define DS4X_ATTN_HEADS 64
 #define DS4X_TOPK_MAX 512
+#define DS4X_MAX_SESSIONS 64
+#define DS4X_PREFILL_MAX_QUERIES 65535
 
 enum {
   DS4X_OK = 0,
@@ -198,6 +200,70 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
                             int32_t k, const uint16_t *q_bf16, float softmax_scale,
                             uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
                             ds4x_stream_t stream);
+
+/*
+ * Micro-batched decode: the CSA indexer score + exact top-k of n_sess
+ * independent sessions in one launch (the sessions' CTAs are split in
+ * proportion to their history lengths; each session is merged by the last
+ * of its CTAs).  Per session exactly ds4x_index_score_topk.
+ *
+ *   idx_rows   device array of n_sess device pointers, session s: u8 [n_rows[s]][68]
+ *   n_rows     device array i64 [n_sess] (a session with n_rows <= 0 gets -1 indices)
+ *   n_sess     1..DS4X_MAX_SESSIONS
+ *   q_bf16     bf16 [n_sess][64][128]
+ *   w          f32 [n_sess][64]
+ *   k          1..512
+ *   out_idx    i32 [n_sess][k], each row as ds4x_index_score_topk's out_idx
+ *   out_score  f32 [n_sess][k] or NULL
+ *   ws         >= ds4x_index_score_topk_batched_workspace(n_sess, k) bytes,
+ *              zero-filled before first use
+ *
+ * Errors: DS4X_EINVAL (pointers, n_sess or k out of range), DS4X_EWORKSPACE.
+ */
+size_t ds4x_index_score_topk_batched_workspace(int32_t n_sess, int32_t k);
+int ds4x_index_score_topk_batched(const uint8_t *const *idx_rows, const int64_t *n_rows, int32_t n_sess,
+                                  const uint16_t *q_bf16, const float *w, int32_t k, int32_t *out_idx,
+                                  float *out_score, void *ws, size_t ws_bytes, ds4x_stream_t stream);
+
+/*
+ * Micro-batched decode attention: ds4x_sparse_attn_decode for n_sess
+ * independent sessions in one launch (grid dimension z = session).
+ *
+ *   kv_rows    device array of n_sess device pointers, session s: u8 [n_rows[s]][583]
+ *   n_rows     device array i64 [n_sess]
+ *   idx        i32 [n_sess][k]
+ *   q_bf16     bf16 [n_sess][64][512]
+ *   out_bf16   bf16 [n_sess][64][512]
+ *   lse        f32 [n_sess][64] or NULL
+ *   ws         >= ds4x_sparse_attn_decode_workspace(k) bytes, zero-filled
+ *              before first use (its status word covers every session)
+ *
+ * Errors: DS4X_EINVAL (pointers, n_sess or k out of range), DS4X_EWORKSPACE.
+ */
+int ds4x_sparse_attn_decode_batched(const uint8_t *const *kv_rows, const int64_t *n_rows, int32_t n_sess,
+                                    const int32_t *idx, int32_t k, const uint16_t *q_bf16, float softmax_scale,
+                                    uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
+                                    ds4x_stream_t stream);
+
+/*
+ * Prefill sparse attention: each of n_queries query tokens attends over its
+ * own k selected rows of one packed KV cache (DS4X README, "Packed prefill
+ * implementation": per-token sparse attention after the batched score/top-k).
+ * Per query exactly ds4x_sparse_attn_decode.
+ *
+ *   kv_rows    u8 [n_rows][583]
+ *   idx        i32 [n_queries][k]
+ *   n_queries  1..DS4X_PREFILL_MAX_QUERIES
+ *   q_bf16     bf16 [n_queries][64][512]
+ *   out_bf16   bf16 [n_queries][64][512]
+ *   lse        f32 [n_queries][64] or NULL
+ *   ws         >= ds4x_sparse_attn_decode_workspace(k) bytes, zero-filled
+ *
+ * Errors: DS4X_EINVAL (pointers, sizes, k out of range), DS4X_EWORKSPACE.
+ */
+int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
+                             int32_t k, const uint16_t *q_bf16, float softmax_scale, uint16_t *out_bf16,
+                             float *lse, void *ws, size_t ws_bytes, ds4x_stream_t stream);
 
 /*
  * Allocation-free form of ds4x_sparse_attn_decode, for callers that cannot

@@ -96,3 +96,25 @@ def test_workspace_calls_reject_null(lib):
     assert lib.ds4x_workspace_init(FAKE, 16, None) == -1
     out = ctypes.c_int32(0)
     assert lib.ds4x_workspace_status(None, None, ctypes.byref(out)) == -1
+
+
+def test_batched_and_prefill_argument_checks(lib):
+    s = ctypes.c_float(0.044)
+    f = lib.ds4x_index_score_topk_batched
+    ws = lib.ds4x_index_score_topk_batched_workspace(16, 512)
+    assert f(None, FAKE, 16, FAKE, FAKE, 512, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 512, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, FAKE, 65, FAKE, FAKE, 512, FAKE, None, FAKE, ws, None) == -1  # beyond DS4X_MAX_SESSIONS
+    assert f(FAKE, FAKE, 16, FAKE, FAKE, 513, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, FAKE, 16, FAKE, FAKE, 512, FAKE, None, FAKE, ws - 1, None) == -3
+    g = lib.ds4x_sparse_attn_decode_batched
+    wa = lib.ds4x_sparse_attn_decode_workspace(512)
+    assert g(FAKE, None, 16, FAKE, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert g(FAKE, FAKE, 0, FAKE, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert g(FAKE, FAKE, 16, FAKE, 512, FAKE, s, FAKE, None, FAKE, wa - 1, None) == -3
+    h = lib.ds4x_sparse_attn_prefill
+    assert h(FAKE, 100, FAKE, 0, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert h(FAKE, 100, FAKE, 65536, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert h(FAKE, 0, FAKE, 8, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert h(FAKE, 100, FAKE + 4, 8, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
+    assert h(FAKE, 100, FAKE, 8, 512, FAKE, s, FAKE, None, FAKE, wa - 1, None) == -3
