@@ -43,6 +43,10 @@ _SIGNATURES = {
                                                         _c_size, _c_p]),
     "ds4x_sparse_attn_prefill": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p,
                                                  _c_size, _c_p]),
+    "ds4x_quantize_query_e4m3": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p]),
+    "ds4x_index_score_topk_prefill_workspace": (_c_size, [_c_i32, _c_i32]),
+    "ds4x_index_score_topk_prefill": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_i32, _c_i64, _c_i32, _c_p, _c_p,
+                                                      _c_p, _c_size, _c_p]),
 }
 
 
@@ -232,3 +236,33 @@ def ds4x_sparse_attn_prefill(kv_rows, n_rows, idx, n_queries, k, q_bf16, softmax
     _check(ws, torch.uint8, "ws")
     _call("ds4x_sparse_attn_prefill", _ptr(kv_rows), int(n_rows), _ptr(idx), int(n_queries), int(k), _ptr(q_bf16),
           float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_quantize_query_e4m3(q, codes, scales, stream=None):
+    """q f32 [..., 128] -> codes u8 [..., 128], scales u8 [..., 4]."""
+    _check(q, torch.float32, "q")
+    n = q.numel() // 128
+    _check(codes, torch.uint8, "codes", numel=n * 128)
+    _check(scales, torch.uint8, "scales", numel=n * 4)
+    _call("ds4x_quantize_query_e4m3", _ptr(q), n, _ptr(codes), _ptr(scales), _stream(stream))
+
+
+def ds4x_index_score_topk_prefill_workspace(n_queries: int, k: int) -> int:
+    return lib().ds4x_index_score_topk_prefill_workspace(int(n_queries), int(k))
+
+
+def ds4x_index_score_topk_prefill(idx_rows, n_rows, q_codes, q_scales, w, n_queries, causal_base, k, out_idx,
+                                  out_score, ws, stream=None):
+    """Per-query exact top-k for a chunk of prefill tokens (query i sees rows
+    t < causal_base + i); q_codes u8 [T, 64, 128], q_scales u8 [T, 64, 4],
+    w f32 [T, 64], out_idx int32 [T, k]."""
+    T = int(n_queries)
+    _check(idx_rows, torch.uint8, "idx_rows", numel=int(n_rows) * 68)
+    _check(q_codes, torch.uint8, "q_codes", numel=T * 64 * 128)
+    _check(q_scales, torch.uint8, "q_scales", numel=T * 64 * 4)
+    _check(w, torch.float32, "w", numel=T * 64)
+    _check(out_idx, torch.int32, "out_idx", numel=T * int(k))
+    _check(out_score, torch.float32, "out_score", numel=T * int(k), allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_index_score_topk_prefill", _ptr(idx_rows), int(n_rows), _ptr(q_codes), _ptr(q_scales), _ptr(w), T,
+          int(causal_base), int(k), _ptr(out_idx), _ptr(out_score), _ptr(ws), ws.numel(), _stream(stream))

@@ -233,4 +233,39 @@ int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32
   return from_cuda(launch_attn_batch(ab, n_queries, ws, stream));
 }
 
+int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, uint8_t *scales,
+                              ds4x_stream_t stream) {
+  if (q == nullptr || codes == nullptr || scales == nullptr) return DS4X_EINVAL;
+  if (!aligned16(q) || !aligned16(codes) || !aligned16(scales)) return DS4X_EINVAL;
+  if (n_vec128 < 1 || n_vec128 > (int64_t(1) << 34)) return DS4X_EINVAL;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  return from_cuda(launch_quantize_query(q, n_vec128, codes, scales, stream));
+}
+
+size_t ds4x_index_score_topk_prefill_workspace(int32_t n_queries, int32_t k) {
+  (void)k;
+  return prefill_ws_bytes(n_queries);
+}
+
+int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
+                                  const uint8_t *q_scales, const float *w, int32_t n_queries, int64_t causal_base,
+                                  int32_t k, int32_t *out_idx, float *out_score, void *ws, size_t ws_bytes,
+                                  ds4x_stream_t stream) {
+  if (idx_rows == nullptr || q_codes == nullptr || q_scales == nullptr || w == nullptr || out_idx == nullptr ||
+      ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(idx_rows) || !aligned16(q_codes) || !aligned16(q_scales) || !aligned16(w) || !aligned16(out_idx) ||
+      !aligned16(ws) || (out_score != nullptr && !aligned16(out_score)))
+    return DS4X_EINVAL;
+  if (n_rows < 1 || n_rows > int64_t(INT32_MAX) || n_queries < 1 || n_queries > DS4X_PREFILL_MAX_QUERIES ||
+      k < 1 || k > DS4X_TOPK_MAX)
+    return DS4X_EINVAL;
+  if (ws_bytes < ds4x_index_score_topk_prefill_workspace(n_queries, k)) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  return from_cuda(launch_score_prefill(idx_rows, n_rows, q_codes, q_scales, w, n_queries, causal_base, k, out_idx,
+                                        out_score, ws, stream));
+}
+
 }  // extern "C"

@@ -140,6 +140,14 @@ struct AttnBatch {
 };
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
 size_t attn_decode_ws_bytes(int32_t k);
+
+// Chunked prefill: query quantiser and the multi-query scorer.
+cudaError_t launch_quantize_query(const float *q, int64_t n_vec, uint8_t *codes, uint8_t *scales,
+                                  cudaStream_t stream);
+size_t prefill_ws_bytes(int32_t T);
+cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
+                                 const uint8_t *q_scales, const float *w, int32_t T, int64_t causal_base,
+                                 int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                int32_t k, const uint16_t *q, float scale, uint16_t *out,
                                float *lse, void *ws, cudaStream_t stream);

@@ -246,6 +246,49 @@ int ds4x_sparse_attn_decode_batched(const uint8_t *const *kv_rows, const int64_t
                                     ds4x_stream_t stream);
 
 /*
+ * Query quantiser for the chunked-prefill scorer: each 128-value vector (one
+ * token, one head) becomes 128 E4M3 codes with one UE8M0 scale per 32 values
+ * (least e with amax <= 448 * 2^e, amax = 0 giving e = 0, e clamped to
+ * [-127, 127]; x / 2^e rounded to nearest, ties to even, sign kept).
+ *
+ *   q          f32 [n_vec128][128]
+ *   codes      u8 [n_vec128][128]
+ *   scales     u8 [n_vec128][4]
+ *
+ * Output bytes are bit-exact with that rule.  Errors: DS4X_EINVAL.
+ */
+int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, uint8_t *scales,
+                              ds4x_stream_t stream);
+
+/*
+ * Chunked-prefill CSA score + per-query exact top-k (DS4X README, "Packed
+ * prefill implementation": batch score/top-k over the packed indexer rows).
+ * Query token i (0..n_queries-1) sees rows t < causal_base + i:
+ *
+ *   s_it = sum_h w[i][h] * max(0, q^[i][h] . k_t),  q^ = E4M3 code * 2^(scale-127)
+ *
+ * and gets the exact top-k of its visible rows (score descending, lower
+ * index first; -1 / NaN past its visible count).  Run as the fused scorer
+ * over one "session" per query token (up to DS4X_MAX_SESSIONS per launch).
+ *
+ *   idx_rows   u8 [n_rows][68]
+ *   q_codes    u8 [n_queries][64][128], q_scales u8 [n_queries][64][4]
+ *              (ds4x_quantize_query_e4m3); scale bytes 4..245 keep q^
+ *              exact in the kernel's bf16 staging
+ *   w          f32 [n_queries][64]
+ *   out_idx    i32 [n_queries][k]; out_score f32 [n_queries][k] or NULL
+ *   ws         >= ds4x_index_score_topk_prefill_workspace(n_queries, k)
+ *              bytes, zero-filled before first use
+ *
+ * Errors: DS4X_EINVAL (pointers, sizes, k), DS4X_EWORKSPACE.
+ */
+size_t ds4x_index_score_topk_prefill_workspace(int32_t n_queries, int32_t k);
+int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
+                                  const uint8_t *q_scales, const float *w, int32_t n_queries, int64_t causal_base,
+                                  int32_t k, int32_t *out_idx, float *out_score, void *ws, size_t ws_bytes,
+                                  ds4x_stream_t stream);
+
+/*
  * Prefill sparse attention: each of n_queries query tokens attends over its
  * own k selected rows of one packed KV cache (DS4X README, "Packed prefill
  * implementation": per-token sparse attention after the batched score/top-k).

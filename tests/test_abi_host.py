@@ -118,3 +118,18 @@ def test_batched_and_prefill_argument_checks(lib):
     assert h(FAKE, 0, FAKE, 8, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
     assert h(FAKE, 100, FAKE + 4, 8, 512, FAKE, s, FAKE, None, FAKE, wa, None) == -1
     assert h(FAKE, 100, FAKE, 8, 512, FAKE, s, FAKE, None, FAKE, wa - 1, None) == -3
+
+
+def test_prefill_scorer_argument_checks(lib):
+    f = lib.ds4x_quantize_query_e4m3
+    assert f(None, 4, FAKE, FAKE, None) == -1
+    assert f(FAKE, 0, FAKE, FAKE, None) == -1
+    assert f(FAKE, 4, FAKE + 4, FAKE, None) == -1
+    g = lib.ds4x_index_score_topk_prefill
+    ws = lib.ds4x_index_score_topk_prefill_workspace(2048, 512)
+    assert ws >= 2048 * 64 * 128 * 2
+    assert g(None, 65536, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws, None) == -1
+    assert g(FAKE, 0, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws, None) == -1
+    assert g(FAKE, 65536, FAKE, FAKE, FAKE, 0, 63488, 512, FAKE, None, FAKE, ws, None) == -1
+    assert g(FAKE, 65536, FAKE, FAKE, FAKE, 2048, 63488, 0, FAKE, None, FAKE, ws, None) == -1
+    assert g(FAKE, 65536, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws - 1, None) == -3
