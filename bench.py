@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode attn step latency (µs/layer) & compressed rows/s vs N; achieved HBM GB/s"
 WORKLOADS = {"tiny": 4096, "mid": 131072, "long": 1048576}
+EXTRA_WORKLOADS = ("sessions", "prefill")  # parity configurations, measured on request
 K_TOP = 512
 HEADS = 64
 FALLBACK_HBM_GBS = 6800.0
@@ -233,12 +234,18 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS) + list(EXTRA_WORKLOADS))
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload in EXTRA_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode workloads only"}))
+            return
+        (run_sessions if args.workload == "sessions" else run_prefill)(args)
+        return
     n = WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, args.workload, n)
@@ -447,6 +454,200 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
 
+
+
+# ---------------------------------------------------------------------------
+# Extra workloads: micro-batched decode and chunked prefill
+# ---------------------------------------------------------------------------
+
+def _gpu_setup():
+    import torch
+
+    from compressed_kv_sparse_csa_gb300 import binding as B
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    return torch, B, dev, torch.cuda.Stream(device=dev)
+
+
+def _timed_graph(torch, stream, graphs, steps):
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    stream.synchronize()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def run_sessions(args):
+    """16 independent decode sessions (lengths uniform on [8192, 65536],
+    seeded), one batched scorer launch and one batched attention launch per
+    step; L layer copies rotated so the indexer rows exceed L2."""
+    import numpy as np
+
+    torch, B, dev, stream = _gpu_setup()
+    rng = np.random.default_rng(1003)
+    n_sess = 16
+    lens = rng.integers(8192, 65536 + 1, size=n_sess)
+    L = max(2, min(args.layers, 6))
+    gen = torch.Generator(device=dev)
+    layers = []
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            gen.manual_seed(3000 + l)
+            idx_t, kv_t = [], []
+            for nr in lens:
+                nr = int(nr)
+                it = torch.empty(nr * 68, dtype=torch.uint8, device=dev)
+                kt = torch.empty(nr * 583, dtype=torch.uint8, device=dev)
+                B.ds4x_cache_append(kt, it, 0, torch.randn((nr, 512), generator=gen, device=dev),
+                                    torch.randn((nr, 128), generator=gen, device=dev), stream=stream)
+                idx_t.append(it)
+                kv_t.append(kt)
+            layers.append({
+                "idx": idx_t, "kv": kv_t,
+                "idx_p": torch.tensor([t.data_ptr() for t in idx_t], dtype=torch.int64, device=dev),
+                "kv_p": torch.tensor([t.data_ptr() for t in kv_t], dtype=torch.int64, device=dev),
+                "n": torch.tensor([int(x) for x in lens], dtype=torch.int64, device=dev),
+                "q": torch.randn((n_sess, 64, 128), generator=gen, device=dev).to(torch.bfloat16),
+                "w": torch.rand((n_sess, 64), generator=gen, device=dev) / 8,
+                "qa": torch.randn((n_sess, 64, 512), generator=gen, device=dev).to(torch.bfloat16),
+                "oi": torch.empty((n_sess, K_TOP), dtype=torch.int32, device=dev),
+                "out": torch.empty((n_sess, 64, 512), dtype=torch.bfloat16, device=dev)})
+        ws_s = torch.empty(B.ds4x_index_score_topk_batched_workspace(n_sess, K_TOP), dtype=torch.uint8, device=dev)
+        ws_a = torch.empty(B.ds4x_sparse_attn_decode_workspace(K_TOP), dtype=torch.uint8, device=dev)
+        B.ds4x_workspace_init(ws_s, stream=stream)
+        B.ds4x_workspace_init(ws_a, stream=stream)
+    stream.synchronize()
+    scale = 1.0 / math.sqrt(512.0)
+
+    def step(c, score_only=False):
+        B.ds4x_index_score_topk_batched(c["idx_p"], c["n"], c["q"], c["w"], K_TOP, c["oi"], None, ws_s, stream=stream)
+        if not score_only:
+            B.ds4x_sparse_attn_decode_batched(c["kv_p"], c["n"], c["oi"], K_TOP, c["qa"], scale, c["out"], None, ws_a,
+                                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(layers[i % L])
+    stream.synchronize()
+    graphs, sgraphs = [], []
+    for c in layers:
+        for lst, so in ((graphs, False), (sgraphs, True)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(c, so)
+            lst.append(g)
+    steps = min(args.steps, 1000)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        ms = _timed_graph(torch, stream, graphs, steps)
+    ms_sc = _timed_graph(torch, stream, sgraphs, steps)
+    total = int(lens.sum())
+    step_b = sum(step_bytes(int(x)) for x in lens)
+    peak, kind = measured_peak()
+    sb = sum(scorer_bytes(int(x)) for x in lens)
+    print(json.dumps({
+        "metric": "micro-batched decode step latency (us) & compressed rows/s",
+        "value": total / (ms * 1e-3), "unit": "compressed rows/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-in/fp32-acc (MXFP4 + E4M3/FP16 packed rows)", "data": "synthetic",
+        "config": {"workload": "16 decode sessions, lengths uniform on [8192, 65536] (seed 1003), batch 1 each",
+                   "rows_total": total, "lengths": [int(x) for x in lens], "top_k": K_TOP, "layer_copies": L,
+                   "us_per_step": ms * 1e3, "step_bytes": step_b,
+                   "step_roofline_frac": step_b / (ms * 1e-3) / 1e9 / peak},
+        "roofline": {"kernel": "ds4x_index_score_topk_batched", "bound": "hbm",
+                     "achieved": sb / (ms_sc * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": sb / (ms_sc * 1e-3) / 1e9 / peak, "traffic": None, "us_per_launch": ms_sc * 1e3,
+                     "peak_kind": kind},
+        "gpu_launches": steps * 2, "clocks": clk.summary()}), flush=True)
+
+
+def run_prefill(args):
+    """One chunk of 2048 prefill query tokens over 65,536 history rows (query
+    i sees rows t < 63,488 + i): query quantiser + per-query causal top-512 +
+    per-query sparse attention."""
+    torch, B, dev, stream = _gpu_setup()
+    T, n, base = 2048, 65536, 63488
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4004)
+    with torch.cuda.stream(stream):
+        idx_rows = torch.empty(n * 68, dtype=torch.uint8, device=dev)
+        kv_rows = torch.empty(n * 583, dtype=torch.uint8, device=dev)
+        B.ds4x_cache_append(kv_rows, idx_rows, 0, torch.randn((n, 512), generator=gen, device=dev),
+                            torch.randn((n, 128), generator=gen, device=dev), stream=stream)
+        q = torch.randn((T, 64, 128), generator=gen, device=dev)
+        w = torch.rand((T, 64), generator=gen, device=dev) / 8
+        qa = torch.randn((T, 64, 512), generator=gen, device=dev).to(torch.bfloat16)
+        codes = torch.empty((T, 64, 128), dtype=torch.uint8, device=dev)
+        scales = torch.empty((T, 64, 4), dtype=torch.uint8, device=dev)
+        oi = torch.empty((T, K_TOP), dtype=torch.int32, device=dev)
+        out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device=dev)
+        ws_s = torch.empty(B.ds4x_index_score_topk_prefill_workspace(T, K_TOP), dtype=torch.uint8, device=dev)
+        ws_a = torch.empty(B.ds4x_sparse_attn_decode_workspace(K_TOP), dtype=torch.uint8, device=dev)
+        B.ds4x_workspace_init(ws_s, stream=stream)
+        B.ds4x_workspace_init(ws_a, stream=stream)
+    stream.synchronize()
+    scale = 1.0 / math.sqrt(512.0)
+
+    def quant():
+        B.ds4x_quantize_query_e4m3(q, codes, scales, stream=stream)
+
+    def score():
+        B.ds4x_index_score_topk_prefill(idx_rows, n, codes, scales, w, T, base, K_TOP, oi, None, ws_s, stream=stream)
+
+    def attend():
+        B.ds4x_sparse_attn_prefill(kv_rows, n, oi, T, K_TOP, qa, scale, out, None, ws_a, stream=stream)
+
+    parts = {}
+    with torch.cuda.stream(stream):
+        for f in (quant, score, attend):
+            f()
+    stream.synchronize()
+    steps = max(1, min(args.steps, 5))
+    for name, fns in (("step", (quant, score, attend)), ("quant", (quant,)), ("score", (score,)),
+                      ("attend", (attend,))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in fns:
+                f()
+        if name == "step":
+            with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+                parts[name] = _timed_graph(torch, stream, [g], steps)
+        else:
+            parts[name] = _timed_graph(torch, stream, [g], steps)
+    pairs = sum(min(n, base + i) for i in range(T))
+    flop_score = pairs * 64 * 128 * 2.0          # q^ . k for every visible (query, row, head)
+    flop_attn = T * 64 * K_TOP * 512 * 2.0 * 2   # logits and weighted sum
+    peak_bf16 = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_bf16 = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        peak_bf16 = 1900.0
+    peak_fp8 = 2.0 * peak_bf16  # FP8 dense nominal rate is twice bf16's
+    print(json.dumps({
+        "metric": "prefill chunk latency (ms) & query tokens/s",
+        "value": T / (parts["step"] * 1e-3), "unit": "query tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": 1, "ms_per_step": parts["step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "E4M3 x E2M1 block-scaled (scorer), bf16-in/fp32-acc (attention)", "data": "synthetic",
+        "config": {"workload": "2048 prefill tokens x 64 heads over 65536 rows, causal base 63488",
+                   "ms_quantize": parts["quant"], "ms_score_topk": parts["score"], "ms_attention": parts["attend"],
+                   "visible_pairs": pairs},
+        "roofline": {"kernel": "ds4x_index_score_topk_prefill", "bound": "tensor",
+                     "achieved": flop_score / (parts["score"] * 1e-3) / 1e12,
+                     "peak": peak_fp8, "unit": "TFLOP/s", "frac": flop_score / (parts["score"] * 1e-3) / 1e12 / peak_fp8,
+                     "peak_kind": "measured bf16 burst x 2 (FP8 nominal ratio)", "traffic": None,
+                     "attention_tflops": flop_attn / (parts["attend"] * 1e-3) / 1e12},
+        "gpu_launches": None, "clocks": clk.summary()}), flush=True)
 
 if __name__ == "__main__":
     main()
