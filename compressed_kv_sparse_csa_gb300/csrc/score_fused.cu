@@ -27,11 +27,16 @@
 //    score bits;
 //  * after the stream one scan of the histogram locates the CTA's 512th and
 //    16th keys; one pass keeps the keys at or above the 512th key's bucket
-//    (a superset of the local top-512) and resolves the exact top-16; the
-//    CTA publishes both; the last CTA to finish merges the CTAs' top-16
-//    sets with a counting sort, fetches the supersets of any CTA whose 16th
-//    key beats the k-th key (so the result is exact for every input) and
-//    writes the outputs.
+//    (a superset of the local top-512) and collects the keys at or above the
+//    16th key's bucket: the CTA's candidates, published unsorted with a
+//    bound that every key it left out is below;
+//  * the CTAs of a session meet at a bounded barrier (the launch is
+//    cooperative, so all are resident); each then loads all the session's
+//    candidates, finds the k-th largest by a radix select, and writes its
+//    own winners at their ranks (counted against all candidates), so the
+//    merge runs in every CTA at once instead of in the last one.  A CTA
+//    whose bound beats the k-th key may hold more winners: then every such
+//    CTA publishes its superset and the session's first CTA merges exactly.
 //
 // The bf16 query q is split per head and 32-element block into E4M3 pieces
 // q = hi * 2^a + lo * 2^b, each with the block-scale rule of the cache writer
@@ -66,8 +71,12 @@ constexpr int kChunkTiles = 64;
 constexpr int kLocalK = DS4X_TOPK_MAX;     // 512
 constexpr int kKeysCap = kLocalK + kChunkTiles * kTileRows;  // 8704
 constexpr int kSelPerThread = 17;          // 17 * 512 >= kKeysCap and >= 256 * 16 + 512
-constexpr int kTopM = 16;
-constexpr int kPubCap = 1024;              // keys a CTA may publish (its top-16, then a superset of the rest)
+constexpr int kTopM = 16;                  // fewest candidates a CTA publishes
+constexpr int kCandCap = kLocalK + 64;     // candidates a CTA may publish (its top M and their bucket)
+constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged CTA may publish
+constexpr int kPoolPer = 8;                // pool keys each selection thread holds in registers
+constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
+constexpr int kRadixBuckets = 2048;        // radix-select histogram over the pool
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
@@ -103,9 +112,13 @@ __device__ __forceinline__ uint32_t op_offset(int r, int kk) {
 struct SelShared {
   unsigned long long red_min[16], red_max[16];
   int red_cnt[16];
-  int scan[16];
-  int bstar, above, bcnt, out_cnt, list_cnt, n16, nb16;
-  int c512_b, c512_above, c16_b, c16_above, c16_cnt, total;
+  alignas(16) int scan[16];
+  uint32_t red_lo[16], red_hi[16];
+  int bstar, above, bcnt, out_cnt, list_cnt;
+  int c512_b, c512_above, cM_b, cM_above, cM_cnt, total;
+  int fill, ncol, wcnt, pub_cnt, n_all, ok;
+  uint32_t base;
+  unsigned long long cut;
 };
 
 struct __align__(1024) Smem {
@@ -114,26 +127,37 @@ struct __align__(1024) Smem {
   unsigned long long keys[kKeysCap];          // [0, 512): carried keys; then the chunk's keys
   unsigned long long out[kLocalK];
   unsigned long long sortbuf[2 * kLocalK];
-  unsigned long long top16[32];
-  unsigned long long b16[32];
+  unsigned long long small[32];               // the radix select's last bucket
   uint32_t hist[kHistWords];                  // fixed histogram, or the adaptive one inside select_top
   alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
   uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
   unsigned long long full[kStages], empty[kStages];
   unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots], dempty[kDSlots];
   SelShared sel;
-  int fetch[kMaxCtas];
+  unsigned long long cand[kCandCap];          // this CTA's candidates
+  unsigned long long th;                      // ... and the bound on the keys it left out
+  uint32_t epoch;                             // the session's exchange count at launch
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
+};
+
+// Per-session exchange words.  A launch with epoch e uses the words of
+// parity e & 1; the session's first CTA clears the other parity (the next
+// exchange's) before it arrives, and advances the epoch once every CTA has
+// arrived, so no word is cleared while a CTA of its exchange still reads it.
+struct alignas(128) SessSync {
+  unsigned long long main[2];  // arrivals << 32 | candidate slots reserved
+  unsigned long long fb[2];    // arrivals at the fallback barrier
+  unsigned long long thm[2];   // largest bound of the session's CTAs
+  uint32_t epoch;              // exchanges completed
 };
 
 struct FusedWs {
   WsHeader hdr;
-  unsigned int tickets[kMaxSess];               // per session: CTAs done (self-resetting)
-  unsigned long long lists[kMaxCtas][kPubCap];  // per CTA: its top-16 (descending), then the rest
-  int cnt[kMaxCtas];                            // entries in the CTA's list
-  unsigned long long th16[kMaxCtas];            // CTA's 16th largest key (0: the list is all it has)
+  SessSync sync[kMaxSess];
+  unsigned long long pool[kMaxCtas * kPubCap];  // session s: slots [cta0 * kPubCap, (cta0 + Gs) * kPubCap)
+  unsigned long long lists[kMaxCtas][kPubCap];  // per CTA, when flagged: its local top-k below its bound
+  int cnt[kMaxCtas];
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -383,130 +407,122 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
   return sh.out_cnt;
 }
 
-// The K largest nonzero keys of keys[0, n) (n <= 4096, distinct, zeros are
-// padding), written to out[0, K') sorted descending, K' = min(K, nonzero
-// count); returns K', or -1 when a bucket is too crowded for this method
-// (the caller then falls back to select_top).  A counting sort: the key range
-// is cut into 4096 power-of-two buckets, a prefix scan over the buckets from
-// the top gives every bucket its first output slot, each key is scattered to
-// that slot plus its arrival order, and keys sharing a bucket re-rank among
-// their bucket-mates.  keys[], hist[] and fill[] (4096 words) are clobbered.
-__device__ int merge_topk_sorted(unsigned long long *keys, int n, int K, unsigned long long *out, uint32_t *hist,
-                                 uint32_t *fill, SelShared &sh, int tid) {
-  constexpr int kB = 4096, kPer = 8, kCrowd = 64;
+// The need-th largest of the distinct nonzero keys that all 512 selection
+// threads hold in v[] and that lie in [lo, hi] (1 <= need <= their count), by
+// radix select: each pass histograms those keys into 2048 buckets spanning
+// [lo, hi] (bucket 0: the top), finds the bucket where the count from the top
+// reaches `need` and narrows [lo, hi] to it; a bucket of at most 32 keys is
+// finished by ranking its keys against each other.  hist[0, 2048) must be
+// zero on entry (and is again on return); sh.ncol must be zero; small holds
+// 32 keys.  Returns the same value in every thread.
+__device__ unsigned long long kth_regs(const unsigned long long (&v)[kPoolPer], unsigned long long lo,
+                                       unsigned long long hi, int need, uint32_t *hist,
+                                       unsigned long long *small, SelShared &sh, int tid) {
+  constexpr int kB = kRadixBuckets;
+  static_assert(kB == 4 * kWGThreads, "four buckets per thread");
   const int lane = tid & 31, warp = tid >> 5;
-  unsigned long long v[kPer];
-  unsigned long long lmin = ~0ull, lmax = 0;
-  int lcnt = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const unsigned long long range = hi - lo;
+    const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 11;  // range >> shift < 2048
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int i = tid + q * kWGThreads;
-    v[q] = i < n ? keys[i] : 0ull;
-    if (v[q] != 0ull) {
-      lmin = min(lmin, v[q]);
-      lmax = max(lmax, v[q]);
-      ++lcnt;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    lmin = min(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
-    lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-    lcnt += __shfl_xor_sync(0xffffffffu, lcnt, o);
-  }
-  if (lane == 0) {
-    sh.red_min[warp] = lmin;
-    sh.red_max[warp] = lmax;
-    sh.red_cnt[warp] = lcnt;
-  }
-  for (int b = tid; b < kB; b += kWGThreads) {
-    hist[b] = 0u;
-    fill[b] = 0u;
-  }
-  bar512();
-  unsigned long long kmin = ~0ull, kmax = 0;
-  int nz = 0;
-  for (int w = 0; w < kWGThreads / 32; ++w) {
-    kmin = min(kmin, sh.red_min[w]);
-    kmax = max(kmax, sh.red_max[w]);
-    nz += sh.red_cnt[w];
-  }
-  const int kout = nz < K ? nz : K;
-  if (kout == 0) return 0;
-  const unsigned long long range = kmax - kmin;
-  const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 12;
-  int bk[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    bk[q] = v[q] != 0ull ? kB - 1 - int((v[q] - kmin) >> shift) : -1;  // bucket 0 holds the highest keys
-    if (bk[q] >= 0) atomicAdd(&hist[bk[q]], 1u);
-  }
-  bar512();
-  // exclusive prefix over the buckets in order 0 (top) .. 4095; thread t owns [8t, 8t + 8)
-  uint32_t c8[8];
-  int local = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    c8[q] = hist[8 * tid + q];
-    local += int(c8[q]);
-  }
-  int incl = local;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sh.scan[warp] = incl;
-  bar512();
-  int first = incl - local, crowd = 0;
-  for (int w = 0; w < warp; ++w) first += sh.scan[w];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (first < kout && int(c8[q]) > kCrowd) crowd = 1;
-    hist[8 * tid + q] = uint32_t(first) | (c8[q] << 16);  // first slot | count
-    first += int(c8[q]);
-  }
-  const int wcrowd = __any_sync(0xffffffffu, crowd);
-  if (lane == 0) sh.red_cnt[warp] = wcrowd;
-  bar512();
-  int crowded = 0;
-  for (int w = 0; w < kWGThreads / 32; ++w) crowded |= sh.red_cnt[w];
-  if (crowded) {
+    for (int q = 0; q < kPoolPer; ++q)
+      if (v[q] != 0ull && v[q] >= lo && v[q] <= hi) atomicAdd(&hist[kB - 1 - int((v[q] - lo) >> shift)], 1u);
     bar512();
-    for (int q = 0; q < kPer; ++q) {  // hand the keys back to the caller
-      const int i = tid + q * kWGThreads;
-      if (i < n) keys[i] = v[q];
+    // thread t owns buckets [4t, 4t + 4); it alone reads them, then clears them
+    const uint4 c4 = reinterpret_cast<const uint4 *>(hist)[tid];
+    reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+    const int local = int(c[0] + c[1] + c[2] + c[3]);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.scan[warp] = incl;
+    bar512();
+    int above = incl - local;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int4 s = reinterpret_cast<const int4 *>(sh.scan)[j];
+      above += (4 * j < warp ? s.x : 0) + (4 * j + 1 < warp ? s.y : 0) + (4 * j + 2 < warp ? s.z : 0) +
+               (4 * j + 3 < warp ? s.w : 0);
+    }
+    if (above < need && above + local >= need) {
+      int acc = above;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (acc < need && acc + int(c[j]) >= need) {
+          sh.bstar = 4 * tid + j;
+          sh.above = acc;
+          sh.bcnt = int(c[j]);
+        }
+        acc += int(c[j]);
+      }
     }
     bar512();
-    return -1;
-  }
-  // scatter every key of a bucket that starts before kout (keys[] is free now)
+    const int bs = sh.bstar, bc = sh.bcnt;
+    need -= sh.above;
+    const unsigned long long blo = lo + (static_cast<unsigned long long>(kB - 1 - bs) << shift);
+    const unsigned long long width_m1 = shift == 0 ? 0ull : ((1ull << shift) - 1ull);
+    const unsigned long long bhi = (hi - blo > width_m1) ? blo + width_m1 : hi;
+    if (bc <= 32) {
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    if (bk[q] < 0) continue;
-    const uint32_t w = hist[bk[q]];
-    const int f = int(w & 0xffffu);
-    if (f < kout) keys[f + int(atomicAdd(&fill[bk[q]], 1u))] = v[q];
+      for (int q = 0; q < kPoolPer; ++q)
+        if (v[q] != 0ull && v[q] >= blo && v[q] <= bhi) {
+          const int slot = atomicAdd(&sh.ncol, 1);
+          if (slot < 32) small[slot] = v[q];
+        }
+      bar512();
+      if (warp == 0) {
+        const unsigned long long x = lane < bc ? small[lane] : 0ull;
+        int r = 0;
+        for (int j = 0; j < bc; ++j) r += small[j] > x;
+        if (lane < bc && r == need - 1) sh.cut = x;
+      }
+      bar512();
+      return sh.cut;
+    }
+    lo = blo;
+    hi = bhi;
   }
-  bar512();
-  // final slots: keys alone in their bucket keep the bucket's slot; others
-  // count the bucket-mates above them
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    if (bk[q] < 0) continue;
-    const uint32_t w = hist[bk[q]];
-    const int f = int(w & 0xffffu), c = int(w >> 16);
-    if (f >= kout) continue;
-    int rank = 0;
-    for (int u = 0; u < c && c > 1; ++u) rank += keys[f + u] > v[q];
-    if (f + rank < kout) out[f + rank] = v[q];
-  }
-  bar512();
-  return kout;
+  return lo;  // not reached for distinct 64-bit keys (each pass keeps <= 2^-11 of the range)
 }
 
-// Cuts of the fixed histogram at the 512 and 16 largest keys: the bucket
-// holding the K-th key, the number of keys in higher buckets and (for K = 16)
-// in that bucket.  b = -1 when there are at most K keys.
-__device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid) {
+// Grid-scope release add and acquire load (the arrival and the poll of the
+// session exchange).
+__device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Thread 0 of a CTA: wait (bounded) until the arrival count in bits 32-63 of
+// *word reaches Gs; returns false (status DS4X_ETIMEOUT) on time-out.
+__device__ bool wait_arrivals(const unsigned long long *word, unsigned int Gs, WsHeader *hdr,
+                              unsigned long long *seen) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    const unsigned long long wv = ld_acquire(word);
+    if (uint32_t(wv >> 32) >= Gs) {
+      *seen = wv;
+      return true;
+    }
+    if (globaltimer() - t0 > kTimeoutNs) {
+      atomicExch(&hdr->status, int32_t(DS4X_ETIMEOUT));
+      return false;
+    }
+  }
+}
+
+// Cuts of the fixed histogram at the 512 and the M largest keys: the bucket
+// holding the K-th key, the number of keys in higher buckets and (for K = M)
+// in that bucket.  b = -1 when there are at most K keys.  Also clears the
+// candidate counter.
+__device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid, int M) {
   const int lane = tid & 31, warp = tid >> 5;
   // thread t owns words [4095 - 8t - 7, 4095 - 8t] = buckets [8191 - 16t - 15, 8191 - 16t]
   uint32_t c[16];
@@ -526,8 +542,10 @@ __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid) {
   if (lane == 31) sh.scan[warp] = incl;
   if (tid == 0) {
     sh.c512_b = -1;
-    sh.c16_b = -1;
-    sh.c16_cnt = 0;
+    sh.cM_b = -1;
+    sh.cM_above = 0;
+    sh.cM_cnt = 0;
+    sh.fill = 0;
   }
   bar512();
   int above = incl - local, total = 0;
@@ -547,13 +565,13 @@ __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid) {
       acc += int(c[q]);
     }
   }
-  if (above < kTopM && above + local >= kTopM) {
+  if (above < M && above + local >= M) {
     int acc = above;
     for (int q = 0; q < 16; ++q) {
-      if (acc + int(c[q]) >= kTopM) {
-        sh.c16_b = bhigh - q;
-        sh.c16_above = acc;
-        sh.c16_cnt = int(c[q]);
+      if (acc + int(c[q]) >= M) {
+        sh.cM_b = bhigh - q;
+        sh.cM_above = acc;
+        sh.cM_cnt = int(c[q]);
         break;
       }
       acc += int(c[q]);
@@ -613,6 +631,20 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   const int n_tiles = int(tile_end - tile_begin);
   WsHeader *hdr = &ws->hdr;
 
+  // tile i of this CTA -> stage i % kStages (producer thread)
+  auto issue_tile = [&](int i) {
+    const int s = i % kStages;
+    const int64_t r0 = (tile_begin + i) * kTileRows;
+    const int nr = n_rows - r0 < kTileRows ? int(n_rows - r0) : kTileRows;
+    const uint32_t bytes = uint32_t(nr) * DS4X_IDX_ROW_BYTES;
+    const uint32_t bulk = bytes & ~15u;
+    const uint8_t *src = rows + r0 * DS4X_IDX_ROW_BYTES;
+    for (uint32_t b = bulk; b < bytes; b += 4)  // ragged tail of the last tile
+      *reinterpret_cast<uint32_t *>(sm.stage[s] + b) = *reinterpret_cast<const uint32_t *>(src + b);
+    mbar_arrive_expect_tx(smem_u32(&sm.full[s]), bulk);
+    bulk_g2s(smem_u32(sm.stage[s]), src, bulk, smem_u32(&sm.full[s]));
+  };
+
   // ---- set-up -------------------------------------------------------------
   if (tid == kProducerWarp * 32) {
     for (int s = 0; s < kStages; ++s) {
@@ -629,6 +661,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     }
     sm.abort_flag = 0;
     fence_mbar_init();
+    // the first tiles go out now, under the set-up below
+    for (int i = 0; i < kStages && i < n_tiles; ++i) issue_tile(i);
+    sm.epoch = __ldcg(&ws->sync[sess].epoch);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
@@ -713,19 +748,10 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   if (warp == kProducerWarp) {
     // ---- producer: bulk-copy tiles into the stage ring ---------------------
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !wait_bar(sm, &sm.empty[s], ((i / kStages) - 1) & 1, hdr)) break;
-        const int64_t r0 = (tile_begin + i) * kTileRows;
-        const int nr = n_rows - r0 < kTileRows ? int(n_rows - r0) : kTileRows;
-        const uint32_t bytes = uint32_t(nr) * DS4X_IDX_ROW_BYTES;
-        const uint32_t bulk = bytes & ~15u;
-        const uint8_t *src = rows + r0 * DS4X_IDX_ROW_BYTES;
-        for (uint32_t b = bulk; b < bytes; b += 4)  // ragged tail of the last tile
-          *reinterpret_cast<uint32_t *>(sm.stage[s] + b) = *reinterpret_cast<const uint32_t *>(src + b);
-        mbar_arrive_expect_tx(smem_u32(&sm.full[s]), bulk);
-        bulk_g2s(smem_u32(sm.stage[s]), src, bulk, smem_u32(&sm.full[s]));
+      int issued = min(kStages, n_tiles);  // issued during the set-up
+      for (int i = issued; i < n_tiles; ++i) {
+        if (!wait_bar(sm, &sm.empty[i % kStages], ((i / kStages) - 1) & 1, hdr)) break;
+        issue_tile(i);
         issued = i + 1;
       }
       if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
@@ -761,7 +787,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     const bool is_conv = warp < 4 * kConvWG;
     const int role_wg = is_conv ? warp / 4 : (warp - 4 * kConvWG) / 4;
     const int n_role_wg = is_conv ? kConvWG : kEpiWG;
-    int carried = 0;  // keys carried from earlier chunks, in keys[0, carried)
+    int last_n_in = 0;  // keys of the last chunk, in keys[0, last_n_in) (carried ones first)
     for (int c0 = 0; c0 < n_tiles; c0 += kChunkTiles) {
       const int c1 = min(n_tiles, c0 + kChunkTiles);
       for (int i = c0 + role_wg; i < c1; i += n_role_wg) {
@@ -831,24 +857,22 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       }
       bar512();
 
-      // ---- end of chunk: keep a superset of the local top-512 ---------------
-      hist_cuts(sm.hist, sm.sel, tid);
+      // ---- end of chunk ---------------------------------------------------------
       const int n_in = kLocalK + (c1 - c0) * kTileRows;
+      if (c1 == n_tiles) {  // the last chunk's keys stay in place for the exchange below
+        last_n_in = n_in;
+        break;
+      }
+      // keep a superset of the local top-512 for the next chunk
+      hist_cuts(sm.hist, sm.sel, tid, kTopM);
       const int b512 = sm.sel.c512_b;  // -1: at most 512 keys, keep all
-      const int b16 = sm.sel.c16_b;    // -1: at most 16 keys
-      const bool last_chunk = c1 == n_tiles;
-      const bool b16_small = b16 < 0 || sm.sel.c16_cnt <= 32;
       unsigned long long v[kSelPerThread];
 #pragma unroll
       for (int qq = 0; qq < kSelPerThread; ++qq) {
         const int i = tid + qq * kWGThreads;
         v[qq] = i < n_in ? sm.keys[i] : 0ull;
       }
-      if (tid == 0) {
-        sm.sel.list_cnt = 0;
-        sm.sel.n16 = 0;
-        sm.sel.nb16 = 0;
-      }
+      if (tid == 0) sm.sel.list_cnt = 0;
       bar512();
       {
         // one shared atomic per warp for the whole pass
@@ -872,186 +896,281 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       }
       bar512();
       int n_keep = sm.sel.list_cnt;
-      if (last_chunk && b16_small) {
-        // the top-16 lies in the kept keys: those above the 16th key's bucket,
-        // and the members of that bucket
-        for (int i0 = 0; i0 < n_keep; i0 += kWGThreads) {
-          const int i = i0 + tid;
-          const unsigned long long key = i < n_keep ? sm.keys[i] : 0ull;
-          const int b = key != 0ull ? fixed_bucket(key) : -2;
-          const bool top = b >= 0 && (b16 < 0 || b > b16);
-          const bool bnd = b >= 0 && b16 >= 0 && b == b16;
-          const int pt = warp_append(&sm.sel.n16, top);
-          const int pb = warp_append(&sm.sel.nb16, bnd);
-          if (top) sm.top16[pt] = key;
-          if (bnd) sm.b16[pb] = key;
-        }
-      }
       for (int i = n_keep + tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
       bar512();
-      if (n_keep > (last_chunk ? kPubCap : kLocalK)) {  // a wide boundary bucket: reduce exactly to 512
+      if (n_keep > kLocalK) {  // a wide boundary bucket: reduce exactly to 512
         const int m = select_top(sm.keys, n_keep, kLocalK, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
         for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = i < m ? sm.out[i] : 0ull;
         bar512();
         n_keep = m;
       }
-      carried = n_keep;
       // histogram of the carried keys for the next chunk
       for (int i = tid; i < kHistWords; i += kWGThreads) sm.hist[i] = 0u;
       bar512();
-      if (!last_chunk) {
-        for (int i = tid; i < carried; i += kWGThreads) hist_add(sm.hist, fixed_bucket(sm.keys[i]));
-        bar512();
-      }
+      for (int i = tid; i < n_keep; i += kWGThreads) hist_add(sm.hist, fixed_bucket(sm.keys[i]));
+      bar512();
     }
 
-    // ---- exact top-16 of this CTA (sorted) and the list it publishes ---------
-    const int m = carried;
-    int n_top;
-    if (m <= kTopM) {
-      n_top = m;
-      if (warp == 0) {
-        const unsigned long long t = warp_sort32_desc(lane < m ? sm.keys[lane] : 0ull, lane);
-        if (lane < kTopM) sm.top16[lane] = t;
-      }
-      bar512();
-    } else if (sm.sel.c16_b >= 0 && sm.sel.c16_cnt <= 32) {
-      // the keys above the 16th key's bucket, plus the best of that bucket
-      const int n_above = sm.sel.n16, need = kTopM - n_above;
-      if (warp == 0) {
-        const unsigned long long bsorted = warp_sort32_desc(lane < sm.sel.nb16 ? sm.b16[lane] : 0ull, lane);
-        const unsigned long long shifted = __shfl_sync(0xffffffffu, bsorted, (lane - n_above) & 31);
-        const unsigned long long cand =
-            lane < n_above ? sm.top16[lane] : (lane < n_above + need ? shifted : 0ull);
-        const unsigned long long srt = warp_sort32_desc(cand, lane);
-        if (lane < kTopM) sm.top16[lane] = srt;
-      }
-      bar512();
-      n_top = kTopM;
-    } else {
-      // a wide 16th-key bucket: exact selection over the kept keys
-      for (int i = tid; i < m; i += kWGThreads) sm.sortbuf[i] = sm.keys[i];
-      bar512();
-      const int n16 = select_top(sm.sortbuf, m, kTopM, sm.top16, sm.hist, sm.keys + kPubCap, sm.sel, tid);
-      if (warp == 0) {
-        const unsigned long long srt = warp_sort32_desc(lane < n16 ? sm.top16[lane] : 0ull, lane);
-        if (lane < kTopM) sm.top16[lane] = srt;
-      }
-      bar512();
-      n_top = kTopM;
-    }
-    const unsigned long long th = (m > kTopM) ? sm.top16[kTopM - 1] : 0ull;
-    const int c = blockIdx.x;
-    for (int i = tid; i < kTopM; i += kWGThreads) ws->lists[c][i] = i < n_top ? sm.top16[i] : 0ull;
-    if (tid == 0) sm.sel.list_cnt = 0;
-    bar512();
-    for (int i0 = 0; i0 < m; i0 += kWGThreads) {
-      const int i = i0 + tid;
-      const unsigned long long key = i < m ? sm.keys[i] : ~0ull;
-      const int p = warp_append(&sm.sel.list_cnt, key < th);
-      if (key < th) ws->lists[c][kTopM + p] = key;
-    }
-    bar512();
-    if (tid == 0) {
-      ws->cnt[c] = kTopM + sm.sel.list_cnt;
-      ws->th16[c] = th;
-    }
-    __threadfence();
-    bar512();
-    if (tid == 0) {
-      const unsigned int ticket = atomicAdd(&ws->tickets[sess], 1u);
-      sm.is_last = (ticket == unsigned(Gs - 1));
-    }
-    bar512();
-
-    if (sm.is_last) {
-      // ---- global merge (last CTA to finish) ----------------------------------
-      __threadfence();
-      const int kk = k;
-      // the CTAs' top-16 lists, then the k largest of them, sorted
-      {
-        unsigned long long cand[8];  // all loads in flight before the stores
+    // ---- this CTA's candidates ------------------------------------------------
+    // The CTA publishes its keys down to the bucket of its M-th key (all of
+    // them when it has few) with a bound th that every key it leaves out is
+    // below.  M covers about k / Gs winners per CTA with a wide margin; any M
+    // gives the exact result, a small one only makes the fallback likelier.
+    if (tid == 0) sm.sel.ok = *reinterpret_cast<volatile int *>(&sm.abort_flag) ? 0 : 1;
+    const int n_in = last_n_in;
+    const float lam = float(k) / float(Gs);
+    const int M = min(k, max(kTopM, int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f))));
+    hist_cuts(sm.hist, sm.sel, tid, M);
+    if (sm.sel.ok) {
+      const int total = sm.sel.total, bM = sm.sel.cM_b;
+      // 0: every key; 1: the keys in buckets >= bM; 2: a crowded bucket, the exact top M
+      const int mode =
+          total <= M + 32 ? 0 : (sm.sel.cM_cnt <= 32 && sm.sel.cM_above + sm.sel.cM_cnt <= kCandCap ? 1 : 2);
+      const int ncand = mode == 0 ? total : (mode == 1 ? sm.sel.cM_above + sm.sel.cM_cnt : M);
+      SessSync &ss = ws->sync[sess];
+      const uint32_t par = sm.epoch & 1u;
+      unsigned long long reserved = 0ull;
+      if (tid == 0 && Gs > 1) reserved = atomicAdd(&ss.main[par], static_cast<unsigned long long>(ncand));
+      if (mode != 2) {
+        unsigned long long v[kSelPerThread];
+        unsigned sel_bits = 0u;  // bit qq: v[qq] is a candidate
+        int cnt = 0;
+        const int bmin = mode == 0 ? 0 : bM;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int i = tid + q * kWGThreads;
-          cand[q] = i < Gs * kTopM ? ld_cg(&ws->lists[cta0 + i / kTopM][i % kTopM]) : 0ull;
+        for (int qq = 0; qq < kSelPerThread; ++qq) {
+          const int i = tid + qq * kWGThreads;
+          v[qq] = i < n_in ? sm.keys[i] : 0ull;
+          const int b = v[qq] != 0ull ? fixed_bucket(v[qq]) : -2;
+          const bool c = b >= bmin;
+          sel_bits |= c ? (1u << qq) : 0u;
+          cnt += __popc(__ballot_sync(0xffffffffu, c));
         }
+        int base = 0;
+        if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.fill, cnt);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sm.keys[tid + q * kWGThreads] = cand[q];
-      }
-      bar512();
-      int sel_n = merge_topk_sorted(sm.keys, Gs * kTopM, kk, sm.out, sm.hist,
-                                    reinterpret_cast<uint32_t *>(sm.stage[0]), sm.sel, tid);
-      bool sorted_ok = sel_n >= 0;
-      if (!sorted_ok) sel_n = select_top(sm.keys, Gs * kTopM, kk, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-      unsigned long long cut = 0ull;
-      if (sel_n == kk) {
-        if (sorted_ok) {
-          cut = sm.out[kk - 1];
-        } else {
-          unsigned long long m0 = ~0ull;
-          for (int i = 0; i < sel_n; ++i) m0 = min(m0, sm.out[i]);
-          cut = m0;
+        for (int qq = 0; qq < kSelPerThread; ++qq) {
+          const bool c = (sel_bits >> qq) & 1u;
+          const unsigned mk = __ballot_sync(0xffffffffu, c);
+          const int p = base + __popc(mk & lt);
+          if (c && p < kCandCap) sm.cand[p] = v[qq];
+          base += __popc(mk);
         }
-      }
-      // CTAs whose 16th key beats the k-th candidate may hold more winners
-      // (select_top above reuses list_cnt, so reset it here)
-      bar512();
-      if (tid == 0) sm.sel.list_cnt = 0;
-      bar512();
-      for (int c0 = 0; c0 < Gs; c0 += kWGThreads) {
-        const int cc = c0 + tid;
-        const unsigned long long t16 = cc < Gs ? ld_cg(&ws->th16[cta0 + cc]) : 0ull;
-        const bool f = t16 != 0ull && t16 > cut;
-        const int p = warp_append(&sm.sel.list_cnt, f);
-        if (f) sm.fetch[p] = cta0 + cc;
-      }
-      bar512();
-      const int n_fetch = min(sm.sel.list_cnt, Gs);
-      if (n_fetch == 0 && sorted_ok) {
-        for (int e = tid; e < kk; e += kWGThreads) {
-          if (e < sel_n) {
-            out_idx[e] = key_index(sm.out[e]);
-            if (out_score) out_score[e] = key_score(sm.out[e]);
-          } else {
-            out_idx[e] = -1;
-            if (out_score) out_score[e] = __uint_as_float(0x7fc00000u);
-          }
-        }
+        // the bucket's floor (bucket 0 also holds everything below it: nothing is left out)
+        if (tid == 0)
+          sm.th = (mode == 0 || bM == 0) ? 0ull
+                                         : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
       } else {
-        // exact fallback: the current winners plus every flagged CTA's list
-        for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
+        unsigned long long *scratch = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
+        for (int i = tid; i < n_in; i += kWGThreads) scratch[i] = sm.keys[i];
         bar512();
-        for (int i = tid; i < sel_n; i += kWGThreads) sm.keys[i] = sm.out[i];
-        int fill = sel_n;
-        bar512();
-        for (int f = 0; f < n_fetch; ++f) {
-          const int cc = sm.fetch[f];
-          const int extra = __ldcg(&ws->cnt[cc]) - kTopM;
-          if (fill + extra > kKeysCap) {
-            sel_n = select_top(sm.keys, fill, kk, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-            for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = i < sel_n ? sm.out[i] : 0ull;
-            fill = sel_n;
-            bar512();
-          }
-          for (int i = tid; i < extra; i += kWGThreads) sm.keys[fill + i] = ld_cg(&ws->lists[cc][kTopM + i]);
-          fill += extra;
-          bar512();
+        select_top(scratch, n_in, M, sm.cand, sm.hist, sm.sortbuf, sm.sel, tid);
+        if (warp == 0) {
+          unsigned long long t = ~0ull;
+          for (int i = lane; i < M; i += 32) t = min(t, sm.cand[i]);
+          for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
+          if (lane == 0) sm.th = t;
         }
-        sel_n = select_top(sm.keys, fill, kk, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-        if (tid == 0) atomicAdd(&hdr->fallback, 1u);
-        const unsigned long long srt = block_sort512_desc(tid < sel_n ? sm.out[tid] : 0ull, sm.sortbuf, tid);
-        if (tid < kk) {
-          if (tid < sel_n) {
-            out_idx[tid] = key_index(srt);
-            if (out_score) out_score[tid] = key_score(srt);
+      }
+      if (tid == 0) sm.sel.base = uint32_t(reserved);
+      bar512();
+
+      // ---- exchange: publish, meet, load the session's candidates ------------------
+      const unsigned long long th = sm.th;
+      unsigned long long *pool_g = ws->pool + size_t(cta0) * kPubCap;
+      if (Gs > 1) {
+        const uint32_t base = sm.sel.base;
+        for (int i = tid; i < ncand; i += kWGThreads) pool_g[base + i] = sm.cand[i];
+        if (tid == 0) atomicMax(&ss.thm[par], th);
+      }
+      reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the radix select's 2048 buckets
+      if (tid == 0) {
+        sm.sel.ncol = 0;
+        sm.sel.wcnt = 0;
+        sm.sel.pub_cnt = 0;
+      }
+      bar512();
+      int n_all = ncand;
+      unsigned long long thmax = th;
+      if (Gs > 1) {
+        if (tid == 0) {
+          if (int(blockIdx.x) == cta0) {  // the next exchange's words: nothing in this launch uses them
+            ss.main[par ^ 1u] = 0ull;
+            ss.fb[par ^ 1u] = 0ull;
+            ss.thm[par ^ 1u] = 0ull;
+          }
+          red_release_add(&ss.main[par], 1ull << 32);
+          unsigned long long seen = 0ull;
+          const bool ok = wait_arrivals(&ss.main[par], unsigned(Gs), hdr, &seen);
+          if (ok && int(blockIdx.x) == cta0) ss.epoch = sm.epoch + 1u;
+          sm.sel.n_all = int(uint32_t(seen));
+          sm.sel.ok = ok ? 1 : 0;
+        }
+        bar512();
+        n_all = sm.sel.n_all;
+        thmax = ld_cg(&ss.thm[par]);
+      }
+      const bool overflow = n_all > kPoolCap;
+      if (sm.sel.ok) {
+        unsigned long long v[kPoolPer];
+#pragma unroll
+        for (int q = 0; q < kPoolPer; ++q) {
+          const int i = tid + q * kWGThreads;
+          v[q] = (!overflow && i < n_all) ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
+        }
+        {
+          unsigned c = 0u, mn = ~0u, mx = 0u;
+#pragma unroll
+          for (int q = 0; q < kPoolPer; ++q)
+            if (v[q] != 0ull) {
+              c += v[q] >= thmax ? 1u : 0u;
+              const uint32_t h = uint32_t(v[q] >> 32);
+              mn = min(mn, h);
+              mx = max(mx, h);
+            }
+          c = __reduce_add_sync(0xffffffffu, c);
+          mn = __reduce_min_sync(0xffffffffu, mn);
+          mx = __reduce_max_sync(0xffffffffu, mx);
+          if (lane == 0) {
+            sm.sel.red_cnt[warp] = int(c);
+            sm.sel.red_lo[warp] = mn;
+            sm.sel.red_hi[warp] = mx;
+          }
+        }
+        bar512();
+        int cnt_ge = 0;
+        uint32_t mn = ~0u, mx = 0u;
+#pragma unroll
+        for (int w = 0; w < kWGThreads / 32; ++w) {
+          cnt_ge += sm.sel.red_cnt[w];
+          mn = min(mn, sm.sel.red_lo[w]);
+          mx = max(mx, sm.sel.red_hi[w]);
+        }
+        // No CTA left out a key above the k-th candidate: the pool holds the
+        // session's top-k.  (One CTA: its candidates always do.)
+        const bool fast = !overflow && (Gs == 1 || (n_all < k ? thmax == 0ull : cnt_ge >= k));
+        if (fast) {
+          unsigned long long cut = 1ull;  // n_all <= k: every candidate wins
+          if (n_all > k) {
+            const unsigned long long lo = max(thmax, static_cast<unsigned long long>(mn) << 32);
+            cut = kth_regs(v, lo, (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull, k, sm.hist, sm.small,
+                           sm.sel, tid);
+          }
+          {  // the winners, every pool key at or above the cut, into out[] (ballots taken twice)
+            int cnt = 0;
+#pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) cnt += __popc(__ballot_sync(0xffffffffu, v[q] != 0ull && v[q] >= cut));
+            int base = 0;
+            if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.wcnt, cnt);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) {
+              const bool win = v[q] != 0ull && v[q] >= cut;
+              const unsigned mk = __ballot_sync(0xffffffffu, win);
+              const int p = base + __popc(mk & lt);
+              if (win && p < kLocalK) sm.out[p] = v[q];
+              base += __popc(mk);
+            }
+          }
+          bar512();
+          const int nwin = min(sm.sel.wcnt, kLocalK);
+          // this CTA's winners, each at its rank among all winners
+          for (int e = warp; e < ncand; e += kWGThreads / 32) {
+            const unsigned long long x = sm.cand[e];
+            if (x < cut) continue;
+            int r = 0;
+            for (int i = lane; i < nwin; i += 32) r += sm.out[i] > x ? 1 : 0;
+            r = __reduce_add_sync(0xffffffffu, r);
+            if (lane == 0 && r < k) {
+              out_idx[r] = key_index(x);
+              if (out_score) out_score[r] = key_score(x);
+            }
+          }
+          if (int(blockIdx.x) == cta0) {
+            for (int e = nwin + tid; e < k; e += kWGThreads) {
+              out_idx[e] = -1;
+              if (out_score) out_score[e] = __uint_as_float(0x7fc00000u);
+            }
+          }
+        } else {
+          // ---- exact fallback -----------------------------------------------------
+          // A CTA whose bound is above the k-th candidate may hold winners it
+          // did not publish: it publishes its local top-k below its bound, and
+          // the session's first CTA merges them with the pool.
+          bool flagged;
+          if (overflow || n_all < k) {
+            flagged = th != 0ull;
           } else {
-            out_idx[tid] = -1;
-            if (out_score) out_score[tid] = __uint_as_float(0x7fc00000u);
+            unsigned c = 0u;
+#pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) c += (v[q] != 0ull && v[q] >= th) ? 1u : 0u;
+            c = __reduce_add_sync(0xffffffffu, c);
+            bar512();
+            if (lane == 0) sm.sel.red_cnt[warp] = int(c);
+            bar512();
+            int s = 0;
+            for (int w = 0; w < kWGThreads / 32; ++w) s += sm.sel.red_cnt[w];
+            flagged = s < k;
+          }
+          int npub = 0;
+          if (flagged) {
+            const int m = select_top(sm.keys, n_in, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+            for (int i0 = 0; i0 < m; i0 += kWGThreads) {
+              const int i = i0 + tid;
+              const unsigned long long x = i < m ? sm.out[i] : 0ull;
+              const bool pub = x != 0ull && x < th;
+              const int p = warp_append(&sm.sel.pub_cnt, pub);
+              if (pub && p < kPubCap) ws->lists[blockIdx.x][p] = x;
+            }
+            bar512();
+            npub = min(sm.sel.pub_cnt, kPubCap);
+          }
+          if (tid == 0) ws->cnt[blockIdx.x] = npub;
+          bar512();
+          if (tid == 0) red_release_add(&ss.fb[par], 1ull << 32);
+          if (int(blockIdx.x) == cta0) {
+            if (tid == 0) {
+              unsigned long long seen = 0ull;
+              sm.sel.ok = wait_arrivals(&ss.fb[par], unsigned(Gs), hdr, &seen) ? 1 : 0;
+              atomicAdd(&hdr->fallback, 1u);
+            }
+            bar512();
+            if (sm.sel.ok) {
+              // the pool and every flagged CTA's list, reduced to the exact top-k
+              int fill = 0;
+              for (int src_i = -1; src_i < Gs; ++src_i) {
+                const unsigned long long *src = src_i < 0 ? pool_g : ws->lists[cta0 + src_i];
+                const int len = src_i < 0 ? (Gs > 1 ? n_all : 0) : min(__ldcg(&ws->cnt[cta0 + src_i]), kPubCap);
+                for (int off = 0; off < len; off += kPubCap) {
+                  const int cl = min(kPubCap, len - off);
+                  if (fill + cl > kKeysCap) {
+                    const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+                    for (int i = tid; i < m; i += kWGThreads) sm.keys[i] = sm.out[i];
+                    bar512();
+                    fill = m;
+                  }
+                  for (int i = tid; i < cl; i += kWGThreads) sm.keys[fill + i] = ld_cg(src + off + i);
+                  fill += cl;
+                  bar512();
+                }
+              }
+              const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+              const unsigned long long srt = block_sort512_desc(tid < m ? sm.out[tid] : 0ull, sm.sortbuf, tid);
+              if (tid < k) {
+                if (tid < m) {
+                  out_idx[tid] = key_index(srt);
+                  if (out_score) out_score[tid] = key_score(srt);
+                } else {
+                  out_idx[tid] = -1;
+                  if (out_score) out_score[tid] = __uint_as_float(0x7fc00000u);
+                }
+              }
+            }
           }
         }
       }
-      if (tid == 0) ws->tickets[sess] = 0u;  // ready for the next call on this workspace
     }
   }
 
@@ -1082,8 +1201,18 @@ cudaError_t launch_score_batch(const ScoreBatch &sb, int64_t tiles_hint, void *w
   // one session: no more CTAs than tiles; a batch: every SM (the kernel splits them)
   const int grid = (tiles_hint > 0 && tiles_hint < cap) ? int(tiles_hint) : cap;
   if (sb.rows_arr != nullptr && grid < sb.n_sess) return cudaErrorInvalidConfiguration;
-  score_fused_kernel<<<grid, kThreads, smem_bytes, stream>>>(sb, static_cast<FusedWs *>(ws));
-  return cudaGetLastError();
+  // cooperative: the CTAs of a session meet at a barrier, so all must be resident
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_fused_kernel, sb, static_cast<FusedWs *>(ws));
 }
 
 cudaError_t launch_score_fused(const uint8_t *idx_rows, int64_t n_rows, const uint16_t *q, const float *w,
