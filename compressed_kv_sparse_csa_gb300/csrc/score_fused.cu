@@ -77,6 +77,9 @@ constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged
 constexpr int kPoolPer = 8;                // pool keys each selection thread holds in registers
 constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
 constexpr int kRadixBuckets = 2048;        // radix-select histogram over the pool
+constexpr int kRankStep = 2;              // candidates ranked together (two lanes store the partials)
+static_assert(kRankStep == 2, "rank partials are stored by lanes 0 and 1");
+constexpr int kDirect = 64;                // up to this many candidates a CTA ranks by direct counts
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
@@ -116,7 +119,7 @@ struct SelShared {
   uint32_t red_lo[16], red_hi[16];
   int bstar, above, bcnt, out_cnt, list_cnt;
   int c512_b, c512_above, cM_b, cM_above, cM_cnt, total;
-  int fill, ncol, wcnt, pub_cnt, n_all, ok;
+  int fill, ncol, wcnt, pub_cnt, n_all, ok, nhi, nge;
   uint32_t base;
   unsigned long long cut;
 };
@@ -128,14 +131,16 @@ struct __align__(1024) Smem {
   unsigned long long out[kLocalK];
   unsigned long long sortbuf[2 * kLocalK];
   unsigned long long small[32];               // the radix select's last bucket
-  uint32_t hist[kHistWords];                  // fixed histogram, or the adaptive one inside select_top
+  alignas(16) uint32_t hist[kHistWords];      // fixed histogram, or the adaptive one inside select_top
   alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
   uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
   unsigned long long full[kStages], empty[kStages];
   unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots], dempty[kDSlots];
+  unsigned long long epoch_full;               // the producer has stored `epoch`
   SelShared sel;
   unsigned long long cand[kCandCap];          // this CTA's candidates
   unsigned long long th;                      // ... and the bound on the keys it left out
+  int rank_part[kWGThreads / 32][kDirect];    // per warp: pool keys above each of its high candidates
   uint32_t epoch;                             // the session's exchange count at launch
   uint32_t tmem_base;
   int abort_flag;
@@ -407,15 +412,15 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
   return sh.out_cnt;
 }
 
-// The need-th largest of the distinct nonzero keys that all 512 selection
-// threads hold in v[] and that lie in [lo, hi] (1 <= need <= their count), by
+// The need-th largest of the distinct nonzero keys of pool[0, n) that lie
+// in [lo, hi] (1 <= need <= their count), by
 // radix select: each pass histograms those keys into 2048 buckets spanning
 // [lo, hi] (bucket 0: the top), finds the bucket where the count from the top
 // reaches `need` and narrows [lo, hi] to it; a bucket of at most 32 keys is
 // finished by ranking its keys against each other.  hist[0, 2048) must be
 // zero on entry (and is again on return); sh.ncol must be zero; small holds
 // 32 keys.  Returns the same value in every thread.
-__device__ unsigned long long kth_regs(const unsigned long long (&v)[kPoolPer], unsigned long long lo,
+__device__ unsigned long long kth_regs(const unsigned long long *pool, int n, unsigned long long lo,
                                        unsigned long long hi, int need, uint32_t *hist,
                                        unsigned long long *small, SelShared &sh, int tid) {
   constexpr int kB = kRadixBuckets;
@@ -425,8 +430,11 @@ __device__ unsigned long long kth_regs(const unsigned long long (&v)[kPoolPer], 
     const unsigned long long range = hi - lo;
     const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 11;  // range >> shift < 2048
 #pragma unroll
-    for (int q = 0; q < kPoolPer; ++q)
-      if (v[q] != 0ull && v[q] >= lo && v[q] <= hi) atomicAdd(&hist[kB - 1 - int((v[q] - lo) >> shift)], 1u);
+    for (int q = 0; q < kPoolPer; ++q) {
+      const int i = q * kWGThreads + tid;
+      const unsigned long long x = i < n ? pool[i] : 0ull;
+      if (x != 0ull && x >= lo && x <= hi) atomicAdd(&hist[kB - 1 - int((x - lo) >> shift)], 1u);
+    }
     bar512();
     // thread t owns buckets [4t, 4t + 4); it alone reads them, then clears them
     const uint4 c4 = reinterpret_cast<const uint4 *>(hist)[tid];
@@ -468,11 +476,14 @@ __device__ unsigned long long kth_regs(const unsigned long long (&v)[kPoolPer], 
     const unsigned long long bhi = (hi - blo > width_m1) ? blo + width_m1 : hi;
     if (bc <= 32) {
 #pragma unroll
-      for (int q = 0; q < kPoolPer; ++q)
-        if (v[q] != 0ull && v[q] >= blo && v[q] <= bhi) {
+      for (int q = 0; q < kPoolPer; ++q) {
+        const int i = q * kWGThreads + tid;
+        const unsigned long long x = i < n ? pool[i] : 0ull;
+        if (x != 0ull && x >= blo && x <= bhi) {
           const int slot = atomicAdd(&sh.ncol, 1);
-          if (slot < 32) small[slot] = v[q];
+          if (slot < 32) small[slot] = x;
         }
+      }
       bar512();
       if (warp == 0) {
         const unsigned long long x = lane < bc ? small[lane] : 0ull;
@@ -524,17 +535,18 @@ __device__ bool wait_arrivals(const unsigned long long *word, unsigned int Gs, W
 // candidate counter.
 __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid, int M) {
   const int lane = tid & 31, warp = tid >> 5;
-  // thread t owns words [4095 - 8t - 7, 4095 - 8t] = buckets [8191 - 16t - 15, 8191 - 16t]
-  uint32_t c[16];
+  // thread t owns words [4095 - 8t - 7, 4095 - 8t] = buckets [8191 - 16t - 15, 8191 - 16t],
+  // read as two 16-byte vectors (word-strided reads would conflict 8 ways)
+  const uint4 lo4 = reinterpret_cast<const uint4 *>(hist)[(kHistWords - 8 - 8 * tid) / 4];
+  const uint4 hi4 = reinterpret_cast<const uint4 *>(hist)[(kHistWords - 4 - 8 * tid) / 4];
+  const uint32_t wd[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // word 4095 - 8t - q
+  // bucket 8191 - 16t - q: the odd (higher) half of word q / 2 first
+  auto count = [&](int q) { return int((q & 1) ? (wd[q >> 1] & 0xffffu) : (wd[q >> 1] >> 16)); };
   int local = 0;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint32_t wv = hist[kHistWords - 1 - 8 * tid - q];
-    c[2 * q] = wv >> 16;  // the odd (higher) bucket of the word first
-    c[2 * q + 1] = wv & 0xffffu;
-    local += int(c[2 * q] + c[2 * q + 1]);
-  }
+  for (int q = 0; q < 8; ++q) local += int((wd[q] >> 16) + (wd[q] & 0xffffu));
   int incl = local;
+#pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
@@ -549,32 +561,41 @@ __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid, int M) {
   }
   bar512();
   int above = incl - local, total = 0;
-  for (int w = 0; w < kWGThreads / 32; ++w) {
-    if (w < warp) above += sh.scan[w];
-    total += sh.scan[w];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int4 sc = reinterpret_cast<const int4 *>(sh.scan)[j];
+    above += (4 * j < warp ? sc.x : 0) + (4 * j + 1 < warp ? sc.y : 0) + (4 * j + 2 < warp ? sc.z : 0) +
+             (4 * j + 3 < warp ? sc.w : 0);
+    total += sc.x + sc.y + sc.z + sc.w;
   }
   const int bhigh = kBuckets - 1 - 16 * tid;
   if (above < kLocalK && above + local >= kLocalK) {
     int acc = above;
+    bool found = false;
+#pragma unroll
     for (int q = 0; q < 16; ++q) {
-      if (acc + int(c[q]) >= kLocalK) {
+      const int cq = count(q);
+      if (!found && acc + cq >= kLocalK) {
+        found = true;
         sh.c512_b = bhigh - q;
         sh.c512_above = acc;
-        break;
       }
-      acc += int(c[q]);
+      acc += cq;
     }
   }
   if (above < M && above + local >= M) {
     int acc = above;
+    bool found = false;
+#pragma unroll
     for (int q = 0; q < 16; ++q) {
-      if (acc + int(c[q]) >= M) {
+      const int cq = count(q);
+      if (!found && acc + cq >= M) {
+        found = true;
         sh.cM_b = bhigh - q;
         sh.cM_above = acc;
-        sh.cM_cnt = int(c[q]);
-        break;
+        sh.cM_cnt = cq;
       }
-      acc += int(c[q]);
+      acc += cq;
     }
   }
   if (tid == 0) sh.total = total;
@@ -642,7 +663,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     for (uint32_t b = bulk; b < bytes; b += 4)  // ragged tail of the last tile
       *reinterpret_cast<uint32_t *>(sm.stage[s] + b) = *reinterpret_cast<const uint32_t *>(src + b);
     mbar_arrive_expect_tx(smem_u32(&sm.full[s]), bulk);
-    bulk_g2s(smem_u32(sm.stage[s]), src, bulk, smem_u32(&sm.full[s]));
+    bulk_g2s_hint(smem_u32(sm.stage[s]), src, bulk, smem_u32(&sm.full[s]), l2_evict_first_policy());
   };
 
   // ---- set-up -------------------------------------------------------------
@@ -659,11 +680,11 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       mbar_init(smem_u32(&sm.dfull[j]), 1);
       mbar_init(smem_u32(&sm.dempty[j]), kTileRows);
     }
+    mbar_init(smem_u32(&sm.epoch_full), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
     // the first tiles go out now, under the set-up below
     for (int i = 0; i < kStages && i < n_tiles; ++i) issue_tile(i);
-    sm.epoch = __ldcg(&ws->sync[sess].epoch);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
@@ -748,12 +769,18 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   if (warp == kProducerWarp) {
     // ---- producer: bulk-copy tiles into the stage ring ---------------------
     if (lane == 0) {
+      // the session's exchange count, needed only after the stream: loaded now,
+      // stored once the copies are out
+      uint32_t epoch;
+      asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(epoch) : "l"(&ws->sync[sess].epoch) : "memory");
       int issued = min(kStages, n_tiles);  // issued during the set-up
       for (int i = issued; i < n_tiles; ++i) {
         if (!wait_bar(sm, &sm.empty[i % kStages], ((i / kStages) - 1) & 1, hdr)) break;
         issue_tile(i);
         issued = i + 1;
       }
+      sm.epoch = epoch;
+      mbar_arrive(smem_u32(&sm.epoch_full));
       if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
         for (int i = max(0, issued - kStages); i < issued; ++i) drain_bar(&sm.full[i % kStages], (i / kStages) & 1);
       }
@@ -916,7 +943,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     // them when it has few) with a bound th that every key it leaves out is
     // below.  M covers about k / Gs winners per CTA with a wide margin; any M
     // gives the exact result, a small one only makes the fallback likelier.
-    if (tid == 0) sm.sel.ok = *reinterpret_cast<volatile int *>(&sm.abort_flag) ? 0 : 1;
+    if (tid == 0) sm.sel.ok = wait_bar(sm, &sm.epoch_full, 0, hdr) && !*reinterpret_cast<volatile int *>(&sm.abort_flag);
     const int n_in = last_n_in;
     const float lam = float(k) / float(Gs);
     const int M = min(k, max(kTopM, int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f))));
@@ -932,30 +959,26 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       unsigned long long reserved = 0ull;
       if (tid == 0 && Gs > 1) reserved = atomicAdd(&ss.main[par], static_cast<unsigned long long>(ncand));
       if (mode != 2) {
-        unsigned long long v[kSelPerThread];
-        unsigned sel_bits = 0u;  // bit qq: v[qq] is a candidate
-        int cnt = 0;
-        const int bmin = mode == 0 ? 0 : bM;
-#pragma unroll
-        for (int qq = 0; qq < kSelPerThread; ++qq) {
-          const int i = tid + qq * kWGThreads;
-          v[qq] = i < n_in ? sm.keys[i] : 0ull;
-          const int b = v[qq] != 0ull ? fixed_bucket(v[qq]) : -2;
-          const bool c = b >= bmin;
-          sel_bits |= c ? (1u << qq) : 0u;
-          cnt += __popc(__ballot_sync(0xffffffffu, c));
-        }
-        int base = 0;
-        if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.fill, cnt);
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-        for (int qq = 0; qq < kSelPerThread; ++qq) {
-          const bool c = (sel_bits >> qq) & 1u;
-          const unsigned mk = __ballot_sync(0xffffffffu, c);
-          const int p = base + __popc(mk & lt);
-          if (c && p < kCandCap) sm.cand[p] = v[qq];
-          base += __popc(mk);
+        // every key at or above the bucket's floor (mode 0: every key); few
+        // qualify, so a warp appends only when one of its lanes has one
+        const unsigned long long thr =
+            (mode == 0 || bM == 0) ? 1ull : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
+        const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(sm.keys);
+        for (int j = tid; 2 * j < n_in; j += kWGThreads) {
+          const ulonglong2 kv = k2[j];  // n_in is even
+          const bool c0 = kv.x >= thr, c1 = kv.y >= thr;
+          if (__any_sync(__activemask(), c0 || c1)) {
+            const unsigned act = __activemask();
+            const unsigned m0 = __ballot_sync(act, c0), m1 = __ballot_sync(act, c1);
+            const int leader = __ffs(act) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&sm.sel.fill, __popc(m0) + __popc(m1));
+            base = __shfl_sync(act, base, leader);
+            const unsigned lt = (1u << lane) - 1u;
+            const int p0 = base + __popc(m0 & lt), p1 = base + __popc(m0) + __popc(m1 & lt);
+            if (c0 && p0 < kCandCap) sm.cand[p0] = kv.x;
+            if (c1 && p1 < kCandCap) sm.cand[p1] = kv.y;
+          }
         }
         // the bucket's floor (bucket 0 also holds everything below it: nothing is left out)
         if (tid == 0)
@@ -987,6 +1010,8 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the radix select's 2048 buckets
       if (tid == 0) {
         sm.sel.ncol = 0;
+        sm.sel.nhi = 0;
+        sm.sel.nge = 0;
         sm.sel.wcnt = 0;
         sm.sel.pub_cnt = 0;
       }
@@ -1013,79 +1038,149 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       }
       const bool overflow = n_all > kPoolCap;
       if (sm.sel.ok) {
-        unsigned long long v[kPoolPer];
-#pragma unroll
-        for (int q = 0; q < kPoolPer; ++q) {
-          const int i = tid + q * kWGThreads;
-          v[q] = (!overflow && i < n_all) ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
-        }
+        // The pool keys at or above the largest bound, compacted into pool_s
+        // (the stage ring is free now): no key below it can be above a
+        // winner, and when none of the CTAs is flagged the winners are among
+        // them.  Their count decides whether any CTA is flagged.
+        unsigned long long *pool_s = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
+        static_assert(kPoolCap * 8 <= kStages * kTileBytes, "the pool fits in the stage ring");
         {
-          unsigned c = 0u, mn = ~0u, mx = 0u;
+          unsigned long long v[kPoolPer];
 #pragma unroll
-          for (int q = 0; q < kPoolPer; ++q)
-            if (v[q] != 0ull) {
-              c += v[q] >= thmax ? 1u : 0u;
+          for (int q = 0; q < kPoolPer; ++q) {
+            const int i = tid + q * kWGThreads;
+            v[q] = (!overflow && i < n_all) ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
+          }
+          unsigned keep = 0u, mn = ~0u, mx = 0u;
+          int cnt = 0;
+#pragma unroll
+          for (int q = 0; q < kPoolPer; ++q) {
+            const bool kq = v[q] != 0ull && v[q] >= thmax;
+            keep |= kq ? (1u << q) : 0u;
+            cnt += __popc(__ballot_sync(0xffffffffu, kq));
+            if (kq) {
               const uint32_t h = uint32_t(v[q] >> 32);
               mn = min(mn, h);
               mx = max(mx, h);
             }
-          c = __reduce_add_sync(0xffffffffu, c);
+          }
+          int base = 0;
+          if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.nge, cnt);
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+          for (int q = 0; q < kPoolPer; ++q) {
+            const bool kq = (keep >> q) & 1u;
+            const unsigned mk = __ballot_sync(0xffffffffu, kq);
+            if (kq) pool_s[base + __popc(mk & lt)] = v[q];
+            base += __popc(mk);
+          }
           mn = __reduce_min_sync(0xffffffffu, mn);
           mx = __reduce_max_sync(0xffffffffu, mx);
           if (lane == 0) {
-            sm.sel.red_cnt[warp] = int(c);
             sm.sel.red_lo[warp] = mn;
             sm.sel.red_hi[warp] = mx;
           }
         }
-        bar512();
-        int cnt_ge = 0;
-        uint32_t mn = ~0u, mx = 0u;
-#pragma unroll
-        for (int w = 0; w < kWGThreads / 32; ++w) {
-          cnt_ge += sm.sel.red_cnt[w];
-          mn = min(mn, sm.sel.red_lo[w]);
-          mx = max(mx, sm.sel.red_hi[w]);
+        // this CTA's candidates at or above the largest bound, into sortbuf
+        for (int e0 = 0; e0 < ncand; e0 += kWGThreads) {
+          const int e = e0 + tid;
+          const unsigned long long x = e < ncand ? sm.cand[e] : 0ull;
+          const bool h = x != 0ull && x >= thmax;
+          const int p = warp_append(&sm.sel.nhi, h);
+          if (h) sm.sortbuf[p] = x;
         }
+        bar512();
+        const int n_ge = sm.sel.nge;
         // No CTA left out a key above the k-th candidate: the pool holds the
         // session's top-k.  (One CTA: its candidates always do.)
-        const bool fast = !overflow && (Gs == 1 || (n_all < k ? thmax == 0ull : cnt_ge >= k));
+        const bool fast = !overflow && (Gs == 1 || (n_all < k ? thmax == 0ull : n_ge >= k));
         if (fast) {
-          unsigned long long cut = 1ull;  // n_all <= k: every candidate wins
-          if (n_all > k) {
-            const unsigned long long lo = max(thmax, static_cast<unsigned long long>(mn) << 32);
-            cut = kth_regs(v, lo, (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull, k, sm.hist, sm.small,
-                           sm.sel, tid);
-          }
-          {  // the winners, every pool key at or above the cut, into out[] (ballots taken twice)
-            int cnt = 0;
+          // Every winner is one of some CTA's candidates at or above the
+          // largest bound, and a candidate wins iff fewer than k pool keys
+          // are above it; its rank is that count.
+          const int nhi = sm.sel.nhi;
+          const int nwin = min(n_all, k);
+          if (nhi <= kDirect) {
+            for (int e0 = 0; e0 < nhi; e0 += kRankStep) {
+              unsigned long long x[kRankStep];
+              unsigned r[kRankStep];
 #pragma unroll
-            for (int q = 0; q < kPoolPer; ++q) cnt += __popc(__ballot_sync(0xffffffffu, v[q] != 0ull && v[q] >= cut));
-            int base = 0;
-            if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.wcnt, cnt);
-            base = __shfl_sync(0xffffffffu, base, 0);
-            const unsigned lt = (1u << lane) - 1u;
+              for (int j = 0; j < kRankStep; ++j) {
+                x[j] = e0 + j < nhi ? sm.sortbuf[e0 + j] : ~0ull;
+                r[j] = 0u;
+              }
 #pragma unroll
-            for (int q = 0; q < kPoolPer; ++q) {
-              const bool win = v[q] != 0ull && v[q] >= cut;
-              const unsigned mk = __ballot_sync(0xffffffffu, win);
-              const int p = base + __popc(mk & lt);
-              if (win && p < kLocalK) sm.out[p] = v[q];
-              base += __popc(mk);
+              for (int q = 0; q < kPoolPer; ++q) {
+                if (q * kWGThreads >= n_ge) break;
+                const int i = q * kWGThreads + tid;
+                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
+#pragma unroll
+                for (int j = 0; j < kRankStep; ++j) r[j] += pv > x[j] ? 1u : 0u;
+              }
+#pragma unroll
+              for (int j = 0; j < kRankStep; ++j) r[j] = __reduce_add_sync(0xffffffffu, r[j]);
+              if (lane < kRankStep && e0 + lane < nhi) sm.rank_part[warp][e0 + lane] = int(lane == 0 ? r[0] : r[1]);
             }
-          }
-          bar512();
-          const int nwin = min(sm.sel.wcnt, kLocalK);
-          // this CTA's winners, each at its rank among all winners
-          for (int e = warp; e < ncand; e += kWGThreads / 32) {
-            const unsigned long long x = sm.cand[e];
-            if (x < cut) continue;
-            int r = 0;
-            for (int i = lane; i < nwin; i += 32) r += sm.out[i] > x ? 1 : 0;
-            r = __reduce_add_sync(0xffffffffu, r);
-            if (lane == 0 && r < k) {
-              out_idx[r] = key_index(x);
-              if (out_score) out_score[r] = key_score(x);
+            bar512();
+            for (int e = tid; e < nhi; e += kWGThreads) {
+              int r = 0;
+#pragma unroll
+              for (int w = 0; w < kWGThreads / 32; ++w) r += sm.rank_part[w][e];
+              if (r < k) {
+                const unsigned long long x = sm.sortbuf[e];
+                out_idx[r] = key_index(x);
+                if (out_score) out_score[r] = key_score(x);
+              }
+            }
+          } else {
+            unsigned long long cut = 1ull;  // n_all <= k: every candidate wins
+            if (n_all > k) {
+              uint32_t mn = ~0u, mx = 0u;
+              for (int w = 0; w < kWGThreads / 32; ++w) {
+                mn = min(mn, sm.sel.red_lo[w]);
+                mx = max(mx, sm.sel.red_hi[w]);
+              }
+              const unsigned long long lo = static_cast<unsigned long long>(mn) << 32;
+              const unsigned long long hi = (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull;
+              cut = kth_regs(pool_s, n_ge, lo, hi, k, sm.hist, sm.small, sm.sel, tid);
+            }
+            {  // the winners, every pool key at or above the cut, into out[] (ballots taken twice)
+              int cnt = 0;
+#pragma unroll
+              for (int q = 0; q < kPoolPer; ++q) {
+                const int i = q * kWGThreads + tid;
+                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
+                cnt += __popc(__ballot_sync(0xffffffffu, pv != 0ull && pv >= cut));
+              }
+              int base = 0;
+              if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.wcnt, cnt);
+              base = __shfl_sync(0xffffffffu, base, 0);
+              const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+              for (int q = 0; q < kPoolPer; ++q) {
+                const int i = q * kWGThreads + tid;
+                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
+                const bool win = pv != 0ull && pv >= cut;
+                const unsigned mk = __ballot_sync(0xffffffffu, win);
+                const int p = base + __popc(mk & lt);
+                if (win && p < kLocalK) sm.out[p] = pv;
+                base += __popc(mk);
+              }
+            }
+            bar512();
+            const int nw = min(sm.sel.wcnt, kLocalK);
+            // this CTA's winners, each at its rank among all winners
+            for (int e = warp; e < ncand; e += kWGThreads / 32) {
+              const unsigned long long x = sm.cand[e];
+              if (x < cut) continue;
+              int r = 0;
+              for (int i = lane; i < nw; i += 32) r += sm.out[i] > x ? 1 : 0;
+              r = __reduce_add_sync(0xffffffffu, r);
+              if (lane == 0 && r < k) {
+                out_idx[r] = key_index(x);
+                if (out_score) out_score[r] = key_score(x);
+              }
             }
           }
           if (int(blockIdx.x) == cta0) {
@@ -1105,7 +1200,11 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           } else {
             unsigned c = 0u;
 #pragma unroll
-            for (int q = 0; q < kPoolPer; ++q) c += (v[q] != 0ull && v[q] >= th) ? 1u : 0u;
+            for (int q = 0; q < kPoolPer; ++q) {  // the whole pool again (pool_s keeps only the top part)
+              const int i = tid + q * kWGThreads;
+              const unsigned long long pv = i < n_all ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
+              c += (pv != 0ull && pv >= th) ? 1u : 0u;
+            }
             c = __reduce_add_sync(0xffffffffu, c);
             bar512();
             if (lane == 0) sm.sel.red_cnt[warp] = int(c);
