@@ -12,11 +12,17 @@
 //      memory, all rows at once, so the gather costs one memory round trip;
 //   2. each warp widens its rows in place to fp16: the E4M3 code values
 //      (exact in fp16, |x| <= 448) and the FP16 RoPE values; the block
-//      scales 2^(e-127) go to a small fp32 table and are applied in fp32
-//      (a power of two, so exactly) to per-block partial sums;
-//   3. logits for 4 heads x 64 rows, the split's softmax statistics
-//      m = max_j l_j, l = sum_j exp(l_j - m) and the unnormalised partial
-//      output o = sum_j exp(l_j - m) v_j;
+//      scales 2^(e-127) go to a small fp32 table;
+//   3. logits for 4 heads x 64 rows on the tensor cores (mma.sync
+//      m16n8k16, fp16 operands, fp32 sums; each head's bf16 query scaled
+//      by a power of two into fp16, exact for every value within 2^24 of
+//      the head's largest), each 64-column partial sum scaled by the
+//      row's block scale in fp32; the split's softmax statistics
+//      m = max_j l_j, l = sum_j exp(l_j - m); the unnormalised partial
+//      output o = sum_j exp(l_j - m) v_j on the tensor cores too, per
+//      64-column block with the weights exp(l_j - m) s_jb / max_j s_jb as
+//      fp16 pairs hi + lo (22 significant bits; the ratio an exact power
+//      of two);
 //   4. the cluster combines its 8 partials through distributed shared
 //      memory, o_h = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s: each CTA
 //      finishes 1/8 of the group's 4 x 512 outputs, and the LSE M + log L.
@@ -36,21 +42,29 @@ constexpr int kHg = 4;                              // heads per cluster
 constexpr int kGroups = DS4X_ATTN_HEADS / kHg;      // 16 clusters
 constexpr int kThreads = 256;
 constexpr int kChunks = 38;                         // 16-byte chunks spanning any 583-byte row
-constexpr int kSlotBytes = 2 * DS4X_KV_DIM + 32;    // 1056: fp16 row + pad (rows 32 B apart mod 128)
+constexpr int kSlotBytes = 2 * DS4X_KV_DIM + 16;    // 1040: fp16 row + pad (8 rows cover all 32 banks)
 constexpr int kGroupsPerRow = DS4X_KV_DIM / 4;      // 128 four-value column groups
 constexpr int kNopeGroups = DS4X_KV_NOPE / 4;       // 112
 constexpr int kBlocks = DS4X_KV_DIM / DS4X_KV_BLOCK;  // 8: 7 scaled E4M3 blocks + the RoPE tail
 constexpr int kNopeBlocks = DS4X_KV_NOPE / DS4X_KV_BLOCK;  // 7
 
-constexpr size_t kKhBytes = size_t(kRows) * kSlotBytes;                // 67,584
-constexpr size_t kQfBytes = size_t(kHg) * DS4X_KV_DIM * sizeof(float);  // 8,192 (then the partial output)
-constexpr size_t kPsBytes = size_t(kRows) * kBlocks * kHg * sizeof(float);  // 8,192
-constexpr size_t kRedBytes = size_t(kHg) * DS4X_KV_DIM * sizeof(float);  // 8,192
-constexpr size_t kSmemBytes = kKhBytes + kQfBytes + kPsBytes + kRedBytes;
+// Tensor-core operands (mma.sync m16n8k16, fp16 in, fp32 accumulate): the
+// query as B of the logits (8 rows: 4 heads and 4 zero rows), the softmax
+// weights as B of the output (per 64-column block, 8 rows of 64 weights,
+// as an fp16 pair hi + lo).
+constexpr int kQhStride = 2 * DS4X_KV_DIM + 16;     // 1040 bytes per query row
+constexpr int kPbStride = 2 * kRows + 16;           // 144 bytes per weight row
+constexpr size_t kKhBytes = size_t(kRows) * kSlotBytes;                     // 66,560
+constexpr size_t kQhBytes = size_t(8) * kQhStride;                          // 8,320
+constexpr size_t kPbBytes = size_t(2) * kBlocks * 8 * kPbStride;            // 18,432: hi and lo parts
+constexpr size_t kOpBytes = size_t(kHg) * DS4X_KV_DIM * sizeof(float);      // 8,192: partial output
+constexpr size_t kRedBytes = size_t(2) * kRows * kHg * sizeof(float);       // 2,048: logit halves
+constexpr size_t kSmemBytes = kKhBytes + kQhBytes + kPbBytes + kOpBytes + kRedBytes;
 static_assert(kRows * kCluster == DS4X_TOPK_MAX, "clusters cover the maximum k");
 static_assert(kChunks * 16 <= kSlotBytes && kSlotBytes % 16 == 0, "a row's bytes fit its slot");
 static_assert(kHg * DS4X_KV_DIM == kThreads * 8, "one 16-byte query load per thread");
 static_assert(kHg * DS4X_KV_DIM == kCluster * kThreads, "one combined output per thread");
+static_assert(kThreads / 32 == kBlocks && kRows == 4 * 16, "warp w: output block w; logits: 4 row tiles x 2 block halves");
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -68,12 +82,42 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t two_codes) {
   asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(two_codes));
   return h2;
 }
-__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t bits) {
-  return __half22float2(*reinterpret_cast<const __half2 *>(&bits));
-}
 // 2^(e - 127) for a UE8M0 code e in 0..254 (e = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float ue8m0_value(uint32_t e) {
   return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// Warp-level tensor-core helpers (fp16 operands from shared memory).
+__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+__device__ __forceinline__ void ldsm_x4_trans(const void *p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+__device__ __forceinline__ void ldsm_x2(const void *p, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+// d += a (16x16, row) * b (16x8, col), fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// 2^e for |e| <= 126 (so that 2^-e is a normal float too).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
+// The query scale exponent of a head whose largest |value| is m: m 2^e lies
+// in [2^14, 2^15) (clamped to |e| <= 126; 0 for an all-zero head).
+__device__ __forceinline__ int query_exp(float m) {
+  if (!(m > 0.f)) return 0;
+  const int e = 14 - (int((__float_as_uint(m) >> 23) & 0xffu) - 127);
+  return e < -126 ? -126 : (e > 126 ? 126 : e);
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -110,14 +154,16 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   uint16_t *__restrict__ out = ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
   float *__restrict__ lse = ab.lse != nullptr ? ab.lse + size_t(bz) * DS4X_ATTN_HEADS : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char *Kh = smem;                                                // [64][1056]: raw, then fp16
-  float *Qf = reinterpret_cast<float *>(smem + kKhBytes);                 // [4][512]
-  float *Opart = Qf;                                                       // [4][512], after the logits
-  float4 *Ps = reinterpret_cast<float4 *>(smem + kKhBytes + kQfBytes);    // [64][8] x 4 heads
-  float *red = reinterpret_cast<float *>(smem + kKhBytes + kQfBytes + kPsBytes);  // [4][512]
+  unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
+  unsigned char *Qh = smem + kKhBytes;                        // [8][1040]: scaled query, fp16
+  unsigned char *Pb = Qh + kQhBytes;                          // [hi, lo][8 blocks][8][144]: weights, fp16
+  float *Opart = reinterpret_cast<float *>(Pb + kPbBytes);    // [4][512]
+  float *red = Opart + kHg * DS4X_KV_DIM;                     // [2][64][4]
   __shared__ __align__(16) float Pt[kRows][kHg];   // logits, then exp(l - m)
   __shared__ float sc[kRows][kBlocks];             // block scales (1 for the RoPE tail)
   __shared__ float ml[2 * kHg];                    // m[4], l[4] of this split
+  __shared__ float qmax[kThreads / 32];            // per warp: largest |q| of its head
+  __shared__ float sbmax[kBlocks];                 // per block: largest row scale
   __shared__ int64_t rows_s[kRows];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -135,16 +181,42 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
     rows_s[tid] = r;
   }
+  // query: thread t holds 8 values of head t / 64 (two warps per head)
+  float qv[8];
   {
     const uint4 qb = reinterpret_cast<const uint4 *>(q + size_t(hg) * kHg * DS4X_KV_DIM)[tid];
     const uint32_t w[4] = {qb.x, qb.y, qb.z, qb.w};
-    float4 *dst = reinterpret_cast<float4 *>(Qf) + 2 * tid;
-    dst[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xffff0000u),
-                         __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xffff0000u));
-    dst[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xffff0000u),
-                         __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xffff0000u));
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qv[2 * i] = __uint_as_float(w[i] << 16);
+      qv[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      m = fmaxf(m, fmaxf(fabsf(qv[2 * i]), fabsf(qv[2 * i + 1])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) qmax[warp] = m;
+  }
+  // the zero rows 4..7 of the query operand and of every weight block
+  for (int i = tid; i < 4 * kQhStride / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(Qh + 4 * kQhStride)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < 2 * kBlocks * 4 * kPbStride / 16; i += kThreads) {
+    const int blk = i / (4 * kPbStride / 16), j = i % (4 * kPbStride / 16);  // blk: part * 8 + block
+    reinterpret_cast<uint4 *>(Pb + blk * 8 * kPbStride + 4 * kPbStride)[j] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
+
+  // Head h's query scaled by 2^e_h so that its largest value lies in
+  // [2^14, 2^15): every bf16 value in that range is exact in fp16, and the
+  // logits are scaled back by 2^-e_h (exactly).
+  const int hq = tid >> 6;
+  {
+    const float s = pow2f(query_exp(fmaxf(qmax[2 * hq], qmax[2 * hq + 1])));
+    __half hv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(qv[i] * s);
+    *reinterpret_cast<uint4 *>(Qh + hq * kQhStride + 16 * (tid & 63)) = *reinterpret_cast<const uint4 *>(hv);
+  }
 
   // 1. gather: chunk c of row rr is bytes [a0 + 16 c, a0 + 16 c + 16), a0 the
   // row's start rounded down to 16; chunks past the row's end are skipped and
@@ -168,98 +240,109 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   cp_async_wait_all();
   __syncthreads();
 
-  // 2. widen in place: warp w owns rows 8w..8w+7.  Every lane reads all its
-  // inputs of a row (column groups lane + 32 q, four values each) before the
-  // warp overwrites the slot with the row's fp16 values.  Skipped rows
-  // become zeros.
+  // 2. widen in place: warp w owns rows 8w..8w+7, two at a time.  Every lane
+  // reads all its inputs of the two rows (column groups lane + 32 q, four
+  // values each) before the warp overwrites the slots with fp16 values.
+  // Skipped rows become zeros with scale 0.
 #pragma unroll 1
-  for (int i = 0; i < kRows / (kThreads / 32); ++i) {
-    const int rr = warp * (kRows / (kThreads / 32)) + i;
-    const int64_t r = rows_s[rr];
-    unsigned char *slot = Kh + rr * kSlotBytes;
-    uint2 *hrow = reinterpret_cast<uint2 *>(slot);
-    if (r < 0) {
+  for (int i = 0; i < kRows / (kThreads / 32); i += 2) {
+    uint32_t in[2][kGroupsPerRow / 32][2];
+    float scale_b[2];
+    int64_t rv[2];
 #pragma unroll
-      for (int q4 = 0; q4 < kGroupsPerRow / 32; ++q4) hrow[lane + 32 * q4] = make_uint2(0u, 0u);
-      if (lane < kBlocks) sc[rr][lane] = 0.f;
-      continue;
-    }
-    const int off = int((r * DS4X_KV_ROW_BYTES) & 15);
-    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(slot);
-    const int sh = (off & 3) * 8;
-    uint32_t in[kGroupsPerRow / 32][2];
+    for (int u = 0; u < 2; ++u) {
+      const int rr = warp * (kRows / (kThreads / 32)) + i + u;
+      rv[u] = rows_s[rr];
+      const unsigned char *slot = Kh + rr * kSlotBytes;
+      const int off = rv[u] >= 0 ? int((rv[u] * DS4X_KV_ROW_BYTES) & 15) : 0;
+      const uint32_t *w32 = reinterpret_cast<const uint32_t *>(slot);
+      const int sh = (off & 3) * 8;
 #pragma unroll
-    for (int q4 = 0; q4 < kGroupsPerRow / 32; ++q4) {
-      const int g = lane + 32 * q4;
-      if (g < kNopeGroups) {  // 4 E4M3 codes
-        const int p = off + 4 * g;
-        in[q4][0] = __funnelshift_r(w32[p >> 2], w32[(p >> 2) + 1], sh);
-        in[q4][1] = 0u;
-      } else {  // 4 FP16 values
-        const int p = off + DS4X_KV_NOPE + 8 * (g - kNopeGroups);
-        const uint32_t a = w32[p >> 2], b = w32[(p >> 2) + 1], c = w32[(p >> 2) + 2];
-        in[q4][0] = __funnelshift_r(a, b, sh);
-        in[q4][1] = __funnelshift_r(b, c, sh);
-      }
-    }
-    float scale_b = 1.f;
-    if (lane < kNopeBlocks) scale_b = ue8m0_value(slot[off + DS4X_KV_NOPE + 2 * DS4X_KV_ROPE + lane]);
-    __syncwarp();
-#pragma unroll
-    for (int q4 = 0; q4 < kGroupsPerRow / 32; ++q4) {
-      const int g = lane + 32 * q4;
-      if (g < kNopeGroups) {
-        hrow[g] = make_uint2(e4m3x2_to_half2_bits(in[q4][0] & 0xffffu), e4m3x2_to_half2_bits(in[q4][0] >> 16));
-      } else {
-        hrow[g] = make_uint2(in[q4][0], in[q4][1]);
-      }
-    }
-    if (lane < kBlocks) sc[rr][lane] = scale_b;
-  }
-  __syncthreads();
-
-  // 3a. logits: thread (row tid / 4, column quarter tid % 4), 4 heads; the
-  // sum over each 64-column block is scaled by the block's scale.
-  {
-    const int r = tid >> 2, jq = tid & 3;
-    const uint2 *K2 = reinterpret_cast<const uint2 *>(Kh + r * kSlotBytes);
-    const float4 *Q4 = reinterpret_cast<const float4 *>(Qf);
-    float a[kHg] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int b = 0; b < kBlocks; ++b) {
-      float part[kHg] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        const int c = jq + 16 * b + 4 * ii;
-        const uint2 hv = K2[c];
-        const float2 x01 = half2_bits_to_float2(hv.x), x23 = half2_bits_to_float2(hv.y);
-#pragma unroll
-        for (int h = 0; h < kHg; ++h) {
-          const float4 y = Q4[h * kGroupsPerRow + c];
-          part[h] = fmaf(y.x, x01.x, part[h]);
-          part[h] = fmaf(y.y, x01.y, part[h]);
-          part[h] = fmaf(y.z, x23.x, part[h]);
-          part[h] = fmaf(y.w, x23.y, part[h]);
+      for (int q4 = 0; q4 < kGroupsPerRow / 32; ++q4) {
+        const int g = lane + 32 * q4;
+        if (g < kNopeGroups) {  // 4 E4M3 codes
+          const int p = off + 4 * g;
+          in[u][q4][0] = __funnelshift_r(w32[p >> 2], w32[(p >> 2) + 1], sh);
+          in[u][q4][1] = 0u;
+        } else {  // 4 FP16 values
+          const int p = off + DS4X_KV_NOPE + 8 * (g - kNopeGroups);
+          const uint32_t a = w32[p >> 2], b = w32[(p >> 2) + 1], c = w32[(p >> 2) + 2];
+          in[u][q4][0] = __funnelshift_r(a, b, sh);
+          in[u][q4][1] = __funnelshift_r(b, c, sh);
         }
       }
-      const float s = sc[r][b];
-#pragma unroll
-      for (int h = 0; h < kHg; ++h) a[h] = fmaf(s, part[h], a[h]);
+      scale_b[u] = 1.f;
+      if (lane < kNopeBlocks) scale_b[u] = ue8m0_value(slot[off + DS4X_KV_NOPE + 2 * DS4X_KV_ROPE + lane]);
     }
+    __syncwarp();
 #pragma unroll
-    for (int h = 0; h < kHg; ++h) {
-      a[h] += __shfl_xor_sync(0xffffffffu, a[h], 1);
-      a[h] += __shfl_xor_sync(0xffffffffu, a[h], 2);
-    }
-    if (jq == 0) {
-      const bool valid = rows_s[r] >= 0;
+    for (int u = 0; u < 2; ++u) {
+      const int rr = warp * (kRows / (kThreads / 32)) + i + u;
+      uint2 *hrow = reinterpret_cast<uint2 *>(Kh + rr * kSlotBytes);
+      const bool valid = rv[u] >= 0;
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) Pt[r][h] = valid ? a[h] * scale : -INFINITY;
+      for (int q4 = 0; q4 < kGroupsPerRow / 32; ++q4) {
+        const int g = lane + 32 * q4;
+        uint2 hv;
+        if (!valid) hv = make_uint2(0u, 0u);
+        else if (g < kNopeGroups)
+          hv = make_uint2(e4m3x2_to_half2_bits(in[u][q4][0] & 0xffffu), e4m3x2_to_half2_bits(in[u][q4][0] >> 16));
+        else
+          hv = make_uint2(in[u][q4][0], in[u][q4][1]);
+        hrow[g] = hv;
+      }
+      if (lane < kBlocks) sc[rr][lane] = valid ? scale_b[u] : 0.f;
     }
   }
   __syncthreads();
 
-  // 3b. split softmax statistics: warp h < 4 takes head h, rows lane, lane + 32.
+  // 3a. logits on the tensor cores: warp w takes rows 16 (w % 4) .. + 16 and
+  // blocks 4 (w / 4) .. + 4; each block's 64-column partial sum is scaled by
+  // the row's block scale.  C fragment: rows g and g + 8 (g = lane / 4),
+  // heads 2 (lane % 4) and + 1 (heads 4..7 are the zero rows).
+  {
+    const int mt = warp & 3, bh = warp >> 2, g = lane >> 2, hc = 2 * (lane & 3);
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
+    const unsigned char *a_base = Kh + (16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8) * kSlotBytes + ((lane >> 4) & 1) * 16;
+    const unsigned char *b_base = Qh + (lane & 7) * kQhStride + ((lane >> 3) & 1) * 16;
+    float tot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      const int blk = 4 * bh + bi;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int k0 = DS4X_KV_BLOCK * blk + 16 * ks;  // columns k0 .. k0 + 15
+        uint32_t af[4], bf[2];
+        ldsm_x4(a_base + 2 * k0, af);
+        ldsm_x2(b_base + 2 * k0, bf);
+        mma_16816(acc, af, bf);
+      }
+      const float s0 = sc[r0][blk], s1 = sc[r1][blk];
+      tot[0] = fmaf(s0, acc[0], tot[0]);
+      tot[1] = fmaf(s0, acc[1], tot[1]);
+      tot[2] = fmaf(s1, acc[2], tot[2]);
+      tot[3] = fmaf(s1, acc[3], tot[3]);
+    }
+    if (hc < kHg) {
+      float *rb = red + bh * kRows * kHg;
+      rb[r0 * kHg + hc] = tot[0];
+      rb[r0 * kHg + hc + 1] = tot[1];
+      rb[r1 * kHg + hc] = tot[2];
+      rb[r1 * kHg + hc + 1] = tot[3];
+    }
+  }
+  __syncthreads();
+  if (tid < kRows * kHg) {
+    const int r = tid / kHg, h = tid % kHg;
+    const float unscale = pow2f(-query_exp(fmaxf(qmax[2 * h], qmax[2 * h + 1])));
+    const float l = (red[r * kHg + h] + red[kRows * kHg + r * kHg + h]) * unscale;
+    Pt[r][h] = rows_s[r] >= 0 ? l * scale : -INFINITY;
+  }
+  __syncthreads();
+
+  // 3b. split softmax statistics: warp h < 4 takes head h, rows lane, lane + 32;
+  // warps 4..7 find each block's largest row scale.
   if (warp < kHg) {
     const int h = warp;
     const float l0 = Pt[lane][h], l1 = Pt[lane + 32][h];
@@ -277,51 +360,66 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       ml[h] = m;
       ml[kHg + h] = s;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int blk = 2 * (warp - kHg) + j;
+      float m = fmaxf(sc[lane][blk], sc[lane + 32][blk]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) sbmax[blk] = m;
+    }
   }
   __syncthreads();
-  // weights per (row, block): exp(l - m) times the block scale
-  for (int e = tid; e < kRows * kBlocks; e += kThreads) {
-    const int r = e / kBlocks, b = e % kBlocks;
-    const float s = sc[r][b];
-    const float4 p = *reinterpret_cast<const float4 *>(&Pt[r][0]);
-    Ps[e] = make_float4(p.x * s, p.y * s, p.z * s, p.w * s);
+  // 3c. output weights per block: exp(l - m) times the row's block scale over
+  // the block's largest (a power of two at most 1, exact), as fp16 hi + lo
+  // (hi the rounded weight, lo the rounded remainder: 22 significant bits)
+  for (int e = tid; e < kBlocks * kHg * kRows; e += kThreads) {
+    const int blk = e / (kHg * kRows), h = (e / kRows) % kHg, r = e % kRows;
+    const float smax = sbmax[blk];
+    const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] / smax) : 0.f;
+    const __half hi = __float2half_rn(w);
+    const __half lo = __float2half_rn(w - __half2float(hi));
+    reinterpret_cast<__half *>(Pb + (blk * 8 + h) * kPbStride)[r] = hi;
+    reinterpret_cast<__half *>(Pb + ((kBlocks + blk) * 8 + h) * kPbStride)[r] = lo;
   }
   __syncthreads();
 
-  // 3c. partial output: thread (column group tid % 128, row half tid / 128).
+  // 3d. partial output on the tensor cores: warp w takes block w (columns
+  // 64 w .. + 64, four 16-column tiles); A = the rows' values transposed, B =
+  // the block's weights; the block's largest scale goes back on at the end.
   {
-    const int c = tid & (kGroupsPerRow - 1), half = tid >> 7, b = c >> 4;
-    float4 acc[kHg];
+    const int blk = warp, g = lane >> 2, hc = 2 * (lane & 3);
+    float acc[4][4];
 #pragma unroll
-    for (int h = 0; h < kHg; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int i = 0; i < kRows / 2; ++i) {
-      const int r = half * (kRows / 2) + i;
-      const uint2 hv = reinterpret_cast<const uint2 *>(Kh + r * kSlotBytes)[c];
-      const float2 v01 = half2_bits_to_float2(hv.x), v23 = half2_bits_to_float2(hv.y);
-      const float4 p = Ps[r * kBlocks + b];
-      const float ph[kHg] = {p.x, p.y, p.z, p.w};
+    for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
-        acc[h].x = fmaf(ph[h], v01.x, acc[h].x);
-        acc[h].y = fmaf(ph[h], v01.y, acc[h].y);
-        acc[h].z = fmaf(ph[h], v23.x, acc[h].z);
-        acc[h].w = fmaf(ph[h], v23.y, acc[h].w);
+      for (int j = 0; j < 4; ++j) acc[t][j] = 0.f;
+    const unsigned char *pb = Pb + blk * 8 * kPbStride + (lane & 7) * kPbStride + ((lane >> 3) & 1) * 16;
+#pragma unroll
+    for (int ks = 0; ks < kRows / 16; ++ks) {
+      uint32_t bh[2], bl[2];
+      ldsm_x2(pb + 32 * ks, bh);
+      ldsm_x2(pb + kBlocks * 8 * kPbStride + 32 * ks, bl);
+      const unsigned char *a_base =
+          Kh + (16 * ks + (lane & 7) + ((lane >> 4) & 1) * 8) * kSlotBytes + ((lane >> 3) & 1) * 16;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint32_t af[4];
+        ldsm_x4_trans(a_base + 2 * (DS4X_KV_BLOCK * blk + 16 * t), af);
+        mma_16816(acc[t], af, bh);
+        mma_16816(acc[t], af, bl);
       }
     }
-    float4 *red4 = reinterpret_cast<float4 *>(red);
-    float4 *O4 = reinterpret_cast<float4 *>(Opart);
-    if (half == 1) {
+    const float smax = sbmax[blk];
+    if (hc < kHg) {
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) red4[h * kGroupsPerRow + c] = acc[h];
-    }
-    __syncthreads();
-    if (half == 0) {
-#pragma unroll
-      for (int h = 0; h < kHg; ++h) {
-        const float4 o = red4[h * kGroupsPerRow + c];
-        O4[h * kGroupsPerRow + c] =
-            make_float4(acc[h].x + o.x, acc[h].y + o.y, acc[h].z + o.z, acc[h].w + o.w);
+      for (int t = 0; t < 4; ++t) {
+        const int d0 = DS4X_KV_BLOCK * blk + 16 * t + g;
+        Opart[hc * DS4X_KV_DIM + d0] = acc[t][0] * smax;
+        Opart[(hc + 1) * DS4X_KV_DIM + d0] = acc[t][1] * smax;
+        Opart[hc * DS4X_KV_DIM + d0 + 8] = acc[t][2] * smax;
+        Opart[(hc + 1) * DS4X_KV_DIM + d0 + 8] = acc[t][3] * smax;
       }
     }
   }
