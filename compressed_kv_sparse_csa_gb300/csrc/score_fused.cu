@@ -13,8 +13,9 @@
 //    four codes per 32-bit column, 32 columns per row; a shift, a mask and a
 //    byte permute per eight codes), and the row's four UE8M0 bytes go to the
 //    row's scale-factor column (six-slot ring);
-//  * warps 17-18 (alternate tiles; a thread that waits on an mbarrier stalls
-//    until its own MMAs drain, so two issuers keep the tensor core busy)
+//  * warps 17-19 (tile i by warp 17 + i % 3; a thread that waits on an
+//    mbarrier stalls until its own MMAs drain, so three issuers keep the
+//    tensor core fed)
 //    issue the tile's eight block-scaled tcgen05.mma kind::mxf8f6f4 (M = 128
 //    rows, N = 64 heads, K = 32; A = E2M1 keys with their own UE8M0 scales,
 //    B = one of the query's two E4M3 pieces with its UE8M0 scales per 32
@@ -62,9 +63,9 @@ constexpr int kConvWG = 2;                 // converter warpgroups: warps 0-7
 constexpr int kEpiWG = 2;                  // epilogue warpgroups: warps 8-15
 constexpr int kWGThreads = 128 * (kConvWG + kEpiWG);  // 512
 constexpr int kProducerWarp = kWGThreads / 32;        // 16
-constexpr int kMmaWarp = kProducerWarp + 1;           // 17: allocates tensor memory; 17-18 issue MMAs
-constexpr int kMmaWarps = 2;                          // tile i is issued by warp kMmaWarp + i % 2
-constexpr int kThreads = kWGThreads + 32 * (1 + kMmaWarps);  // 608
+constexpr int kMmaWarp = kProducerWarp + 1;           // 17: allocates tensor memory; 17-19 issue MMAs
+constexpr int kMmaWarps = 3;                          // tile i is issued by warp kMmaWarp + i % 3
+constexpr int kThreads = kWGThreads + 32 * (1 + kMmaWarps);  // 640
 constexpr int kASlots = 6;                 // tensor-memory A ring
 constexpr int kDSlots = 4;                 // tensor-memory accumulator ring
 constexpr int kChunkTiles = 64;
@@ -103,7 +104,6 @@ static_assert(kDSlots * 64 <= int(kACol0) && kACol0 + 32 * kASlots <= kSfaCol0 &
 static_assert(kSfaCol0 % 4 == 0 && kSfbCol % 4 == 0 && kSfbLoCol % 4 == 0,
               "scale-factor columns start on a 4-column boundary");
 static_assert(kSelPerThread * kWGThreads >= kKeysCap, "selection registers cover the key buffer");
-static_assert(kDSlots % kMmaWarps == 0, "each MMA warp owns its own accumulator slots");
 constexpr int kMaxDynSmem = 232448;         // 227 KB per CTA on sm_103
 
 // Byte offset of (row r, K element kk) in a canonical no-swizzle K-major
@@ -786,7 +786,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       }
     }
   } else if (warp >= kMmaWarp) {
-    // ---- MMA issuers: warp kMmaWarp + m takes tiles m, m + 2, ... ------------
+    // ---- MMA issuers: warp kMmaWarp + m takes tiles m, m + 3, ... ------------
     if (lane == 0) {
       const uint64_t bdesc_hi = smem_desc_noswizzle(smem_u32(sm.bq), kLbo, kSbo);
       const uint64_t bdesc_lo = smem_desc_noswizzle(smem_u32(sm.bq + op_offset(DS4X_IDX_HEADS, 0)), kLbo, kSbo);
