@@ -169,6 +169,16 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, hg = blockIdx.y;
 
+  // the zero rows 4..7 of the query operand and of every weight block
+  for (int i = tid; i < 4 * kQhStride / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(Qh + 4 * kQhStride)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < 2 * kBlocks * 4 * kPbStride / 16; i += kThreads) {
+    const int blk = i / (4 * kPbStride / 16), j = i % (4 * kPbStride / 16);  // blk: part * 8 + block
+    reinterpret_cast<uint4 *>(Pb + blk * 8 * kPbStride + 4 * kPbStride)[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // Launched as a programmatic dependent of the previous kernel (the scorer
+  // that wrote idx): everything above reads no input; wait for it here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid < kRows) {
     const int j = split * kRows + tid;
     int64_t r = -1;
@@ -196,13 +206,6 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) qmax[warp] = m;
-  }
-  // the zero rows 4..7 of the query operand and of every weight block
-  for (int i = tid; i < 4 * kQhStride / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(Qh + 4 * kQhStride)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = tid; i < 2 * kBlocks * 4 * kPbStride / 16; i += kThreads) {
-    const int blk = i / (4 * kPbStride / 16), j = i % (4 * kPbStride / 16);  // blk: part * 8 + block
-    reinterpret_cast<uint4 *>(Pb + blk * 8 * kPbStride + 4 * kPbStride)[j] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
 
@@ -461,9 +464,20 @@ cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStre
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = set_max_smem_once(attn_decode_kernel, int(kSmemBytes), smem_set);
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<<<dim3(kCluster, kGroups, batch), kThreads, kSmemBytes, stream>>>(ab,
-                                                                                      static_cast<WsHeader *>(ws));
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the CTAs may start while the previous
+  // kernel finishes (it lets them go from its tail); the kernel waits for it
+  // before reading anything.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kCluster, kGroups, unsigned(batch));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, ab, static_cast<WsHeader *>(ws));
 }
 
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

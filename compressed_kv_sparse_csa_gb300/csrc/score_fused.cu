@@ -938,6 +938,11 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       bar512();
     }
 
+    // The next kernel in the stream (the attention, launched as a programmatic
+    // dependent) may take an SM as soon as this grid's CTAs leave; it waits
+    // for the whole grid before it reads the indices.
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- this CTA's candidates ------------------------------------------------
     // The CTA publishes its keys down to the bucket of its M-th key (all of
     // them when it has few) with a bound th that every key it leaves out is
