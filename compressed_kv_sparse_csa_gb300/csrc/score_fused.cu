@@ -99,6 +99,15 @@ constexpr uint32_t kIdesc = idesc_mxf8f6f4_e2m1_e4m3(kN);
 constexpr unsigned long long kTimeoutNs = 500ull * 1000 * 1000;  // a bounded wait gives up after 0.5 s
 constexpr uint32_t kWaitHintNs = 2000;     // a waiting thread may sleep in hardware up to 2 us per poll
 constexpr uint32_t kBarSel = 1;            // named barrier of the 512 warpgroup threads
+constexpr uint32_t kBarEpi0 = 2;           // epilogue warpgroup e: named barrier kBarEpi0 + e (128 threads)
+// An mbarrier parity wait for phase c passes early if phase c - 1 is still
+// open, so each parity wait below is done by a thread (or warpgroup) that also
+// waited for the slot's previous phase: the slot counts are multiples of the
+// waiters' rotation.  The MMA warps' wait for a free accumulator slot (three
+// issuers, four slots) uses a monotonic counter instead (dfree).
+static_assert(kStages % kConvWG == 0, "a stage's phases are waited on by one converter warpgroup");
+static_assert(kASlots % kMmaWarps == 0 && kASlots % kConvWG == 0, "an A slot's phases: one issuer, one converter WG");
+static_assert(kDSlots % kEpiWG == 0, "an accumulator slot's full phases: one epilogue warpgroup");
 static_assert(kDSlots * 64 <= int(kACol0) && kACol0 + 32 * kASlots <= kSfaCol0 && kSfbLoCol + 4 <= uint32_t(kTmemCols),
               "tensor-memory map");
 static_assert(kSfaCol0 % 4 == 0 && kSfbCol % 4 == 0 && kSfbLoCol % 4 == 0,
@@ -135,7 +144,8 @@ struct __align__(1024) Smem {
   alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
   uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
   unsigned long long full[kStages], empty[kStages];
-  unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots], dempty[kDSlots];
+  unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots];
+  int dfree[kDSlots];                         // last tile whose epilogue released the slot (-1: none)
   unsigned long long epoch_full;               // the producer has stored `epoch`
   SelShared sel;
   unsigned long long cand[kCandCap];          // this CTA's candidates
@@ -179,6 +189,32 @@ __device__ bool wait_bar(Smem &sm, unsigned long long *bar, uint32_t parity, WsH
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait_sleep(b, parity, kWaitHintNs)) return true;
+    if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      atomicExch(&hdr->status, int32_t(DS4X_ETIMEOUT));
+      *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void st_release_shared(int *p, int v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Bounded wait until the monotonic counter *p reaches target (same time-out
+// and abort rules as wait_bar).
+__device__ bool wait_seq(Smem &sm, const int *p, int target, WsHeader *hdr) {
+  if (ld_acquire_shared(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int it = 0; it < 64; ++it)
+      if (ld_acquire_shared(p) >= target) return true;
     if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) return false;
     if (globaltimer() - t0 > kTimeoutNs) {
       atomicExch(&hdr->status, int32_t(DS4X_ETIMEOUT));
@@ -678,7 +714,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     }
     for (int j = 0; j < kDSlots; ++j) {
       mbar_init(smem_u32(&sm.dfull[j]), 1);
-      mbar_init(smem_u32(&sm.dempty[j]), kTileRows);
+      sm.dfree[j] = -1;
     }
     mbar_init(smem_u32(&sm.epoch_full), 1);
     sm.abort_flag = 0;
@@ -794,7 +830,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       for (int i = warp - kMmaWarp; i < n_tiles; i += kMmaWarps) {
         const int a = i % kASlots, d = i % kDSlots;
         if (!wait_bar(sm, &sm.afull[a], (i / kASlots) & 1, hdr)) break;
-        if (i >= kDSlots && !wait_bar(sm, &sm.dempty[d], ((i / kDSlots) - 1) & 1, hdr)) break;
+        if (i >= kDSlots && !wait_seq(sm, &sm.dfree[d], i - kDSlots, hdr)) break;
         tc_fence_after();
         mma_mxf8f6f4_ta_k128_2b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a), bdesc_hi,
                                 bdesc_lo, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a), tmem_base + kSfbCol,
@@ -859,8 +895,10 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
             tc_ld_x16(d_t + uint32_t(32 * half + 16), v1);
             tc_wait_ld();
             if (half == 1) {
+              // the warpgroup has read the slot: its first thread publishes the tile
               tc_fence_before();
-              mbar_arrive(smem_u32(&sm.dempty[d]));
+              named_bar_sync(kBarEpi0 + uint32_t(role_wg), 128);
+              if (r == 0) st_release_shared(&sm.dfree[d], i);
             }
 #pragma unroll
             for (int g = 0; g < 8; ++g) {  // heads 32 half + 4 g .. + 3
