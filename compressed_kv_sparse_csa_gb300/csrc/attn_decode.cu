@@ -164,6 +164,8 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   __shared__ float ml[2 * kHg];                    // m[4], l[4] of this split
   __shared__ float qmax[kThreads / 32];            // per warp: largest |q| of its head
   __shared__ float sbmax[kBlocks];                 // per block: largest row scale
+  __shared__ float fw[kHg][kCluster];              // combine weights e^(m_s - M) per head and split
+  __shared__ float fl[kHg];                        // ... and their sum L per head
   __shared__ int64_t rows_s[kRows];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -209,18 +211,6 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   }
   __syncthreads();
 
-  // Head h's query scaled by 2^e_h so that its largest value lies in
-  // [2^14, 2^15): every bf16 value in that range is exact in fp16, and the
-  // logits are scaled back by 2^-e_h (exactly).
-  const int hq = tid >> 6;
-  {
-    const float s = pow2f(query_exp(fmaxf(qmax[2 * hq], qmax[2 * hq + 1])));
-    __half hv[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(qv[i] * s);
-    *reinterpret_cast<uint4 *>(Qh + hq * kQhStride + 16 * (tid & 63)) = *reinterpret_cast<const uint4 *>(hv);
-  }
-
   // 1. gather: chunk c of row rr is bytes [a0 + 16 c, a0 + 16 c + 16), a0 the
   // row's start rounded down to 16; chunks past the row's end are skipped and
   // a chunk crossing the end of the buffer is read byte by byte.
@@ -240,20 +230,31 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
         if (src + b < total) dst[b] = kv[src + b];
     }
   }
+  // while the rows are in flight: head h's query scaled by 2^e_h so that its
+  // largest value lies in [2^14, 2^15): every bf16 value in that range is
+  // exact in fp16, and the logits are scaled back by 2^-e_h (exactly)
+  {
+    const int hq = tid >> 6;
+    const float s = pow2f(query_exp(fmaxf(qmax[2 * hq], qmax[2 * hq + 1])));
+    __half hv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(qv[i] * s);
+    *reinterpret_cast<uint4 *>(Qh + hq * kQhStride + 16 * (tid & 63)) = *reinterpret_cast<const uint4 *>(hv);
+  }
   cp_async_wait_all();
   __syncthreads();
 
-  // 2. widen in place: warp w owns rows 8w..8w+7, two at a time.  Every lane
-  // reads all its inputs of the two rows (column groups lane + 32 q, four
+  // 2. widen in place: warp w owns rows 8w..8w+7, four at a time.  Every lane
+  // reads all its inputs of the four rows (column groups lane + 32 q, four
   // values each) before the warp overwrites the slots with fp16 values.
   // Skipped rows become zeros with scale 0.
 #pragma unroll 1
-  for (int i = 0; i < kRows / (kThreads / 32); i += 2) {
-    uint32_t in[2][kGroupsPerRow / 32][2];
-    float scale_b[2];
-    int64_t rv[2];
+  for (int i = 0; i < kRows / (kThreads / 32); i += 4) {
+    uint32_t in[4][kGroupsPerRow / 32][2];
+    float scale_b[4];
+    int64_t rv[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int rr = warp * (kRows / (kThreads / 32)) + i + u;
       rv[u] = rows_s[rr];
       const unsigned char *slot = Kh + rr * kSlotBytes;
@@ -279,7 +280,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
     __syncwarp();
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int rr = warp * (kRows / (kThreads / 32)) + i + u;
       uint2 *hrow = reinterpret_cast<uint2 *>(Kh + rr * kSlotBytes);
       const bool valid = rv[u] >= 0;
@@ -427,31 +428,38 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
   }
 
-  // 4. combine the cluster's 8 partials through distributed shared memory.
+  // 4. combine the cluster's 8 partials through distributed shared memory:
+  // warp 0 turns the 8 splits' (m, l) into each head's weights
+  // f_s = e^(m_s - M), the sum L = sum_s f_s l_s and the LSE; then every
+  // thread reads its 8 partial outputs and divides sum_s f_s o_s by L.
   cluster_sync();
+  if (warp == 0) {
+    // lane = split s (8) x head h (4)
+    const int s = lane & (kCluster - 1), h = lane >> 3;
+    const float ms = ld_peer(&ml[h], uint32_t(s)), ls = ld_peer(&ml[kHg + h], uint32_t(s));
+    float M = ms;
+#pragma unroll
+    for (int o = 1; o < kCluster; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+    float L = f * ls;
+#pragma unroll
+    for (int o = 1; o < kCluster; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    fw[h][s] = f;
+    if (s == 0) fl[h] = L;
+    if (s == 0 && lse != nullptr && cluster_rank() == 0) lse[hg * kHg + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  }
+  __syncthreads();
   {
     const int e = int(cluster_rank()) * kThreads + tid;
     const int h = e / DS4X_KV_DIM, d = e % DS4X_KV_DIM;
-    float ms[kCluster], ls[kCluster], os[kCluster];
+    float os[kCluster];
 #pragma unroll
-    for (int s = 0; s < kCluster; ++s) {
-      ms[s] = ld_peer(&ml[h], uint32_t(s));
-      ls[s] = ld_peer(&ml[kHg + h], uint32_t(s));
-      os[s] = ld_peer(&Opart[h * DS4X_KV_DIM + d], uint32_t(s));
-    }
-    float M = -INFINITY;
+    for (int s = 0; s < kCluster; ++s) os[s] = ld_peer(&Opart[h * DS4X_KV_DIM + d], uint32_t(s));
+    float o = 0.f;
 #pragma unroll
-    for (int s = 0; s < kCluster; ++s) M = fmaxf(M, ms[s]);
-    float L = 0.f, o = 0.f;
-#pragma unroll
-    for (int s = 0; s < kCluster; ++s) {
-      const float f = ms[s] == -INFINITY ? 0.f : expf(ms[s] - M);
-      L = fmaf(f, ls[s], L);
-      o = fmaf(f, os[s], o);
-    }
-    const int head = hg * kHg + h;
-    out[size_t(head) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
-    if (lse != nullptr && d == 0) lse[head] = L > 0.f ? M + logf(L) : -INFINITY;
+    for (int s = 0; s < kCluster; ++s) o = fmaf(fw[h][s], os[s], o);
+    const float L = fl[h];
+    out[size_t(hg * kHg + h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
   }
   cluster_wait_peers();  // peers may still be reading this CTA's partials
 }
