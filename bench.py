@@ -199,6 +199,23 @@ def cpu_baseline(n_rows=262144, reps=5):
                       f"long-decode distribution, numpy float64, 1 thread; {t:.2f} s each"}
 
 
+def max_over_ranks(values, dist, device):
+    """Each timed quantity's maximum over the ranks (the job is as slow as
+    its slowest replica); unchanged on one process."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(world, n_rows, ms_per_step):
+    """Whole-job throughput: every replica scores n_rows per step."""
+    return world * n_rows / (ms_per_step * 1e-3)
+
+
 def reference_arm(args, workload, n):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -429,10 +446,7 @@ def main():
     ms_step = ms_total / args.steps
     ms_sc = ms_score / args.steps
     ms_e2e_step = ms_e2e / e2e_steps
-    if dist is not None:
-        t = torch.tensor([ms_step, ms_sc, ms_e2e_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_sc, ms_e2e_step = t.tolist()
+    ms_step, ms_sc, ms_e2e_step = max_over_ranks([ms_step, ms_sc, ms_e2e_step], dist, dev)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -444,7 +458,7 @@ def main():
     traffic, tnote = recorded_traffic("ds4x_index_score_topk")
     line = {
         "metric": METRIC,
-        "value": world * n / (ms_step * 1e-3),
+        "value": job_value(world, n, ms_step),
         "unit": "compressed rows/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -469,7 +483,7 @@ def main():
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "traffic_note": tnote, "algorithmic_bytes_per_launch": sb, "us_per_launch": ms_sc * 1e3},
-        "e2e": {"value": world * n / (ms_e2e_step * 1e-3), "unit": "compressed rows/s",
+        "e2e": {"value": job_value(world, n, ms_e2e_step), "unit": "compressed rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": ms_e2e_step,
                 "path": "per step one CUDA graph of the public calls: one pinned-host-to-device copy of the "
