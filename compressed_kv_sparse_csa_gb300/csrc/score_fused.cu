@@ -78,8 +78,7 @@ constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged
 constexpr int kPoolPer = 8;                // pool keys each selection thread holds in registers
 constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
 constexpr int kRadixBuckets = 2048;        // radix-select histogram over the pool
-constexpr int kRankStep = 2;              // candidates ranked together (two lanes store the partials)
-static_assert(kRankStep == 2, "rank partials are stored by lanes 0 and 1");
+constexpr int kRankStep = 8;              // candidates ranked together (lane j stores candidate j's partial)
 constexpr int kDirect = 64;                // up to this many candidates a CTA ranks by direct counts
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
@@ -1163,7 +1162,10 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
               }
 #pragma unroll
               for (int j = 0; j < kRankStep; ++j) r[j] = __reduce_add_sync(0xffffffffu, r[j]);
-              if (lane < kRankStep && e0 + lane < nhi) sm.rank_part[warp][e0 + lane] = int(lane == 0 ? r[0] : r[1]);
+              unsigned mine = 0u;
+#pragma unroll
+              for (int j = 0; j < kRankStep; ++j) mine = lane == j ? r[j] : mine;
+              if (lane < kRankStep && e0 + lane < nhi) sm.rank_part[warp][e0 + lane] = int(mine);
             }
             bar512();
             for (int e = tid; e < nhi; e += kWGThreads) {
