@@ -79,7 +79,7 @@ constexpr int kPoolPer = 8;                // pool keys each selection thread ho
 constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
 constexpr int kRadixBuckets = 2048;        // radix-select histogram over the pool
 constexpr int kRankStep = 8;              // candidates ranked together (lane j stores candidate j's partial)
-constexpr int kDirect = 64;                // up to this many candidates a CTA ranks by direct counts
+constexpr int kDirect = 256;               // up to this many candidates a CTA ranks by direct counts
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
@@ -149,7 +149,6 @@ struct __align__(1024) Smem {
   SelShared sel;
   unsigned long long cand[kCandCap];          // this CTA's candidates
   unsigned long long th;                      // ... and the bound on the keys it left out
-  int rank_part[kWGThreads / 32][kDirect];    // per warp: pool keys above each of its high candidates
   uint32_t epoch;                             // the session's exchange count at launch
   uint32_t tmem_base;
   int abort_flag;
@@ -992,9 +991,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     hist_cuts(sm.hist, sm.sel, tid, M);
     if (sm.sel.ok) {
       const int total = sm.sel.total, bM = sm.sel.cM_b;
-      // 0: every key; 1: the keys in buckets >= bM; 2: a crowded bucket, the exact top M
+      // 0: every key; 1: the keys in buckets >= bM; 2: more than kCandCap of those, the exact top M
       const int mode =
-          total <= M + 32 ? 0 : (sm.sel.cM_cnt <= 32 && sm.sel.cM_above + sm.sel.cM_cnt <= kCandCap ? 1 : 2);
+          total <= M + 32 ? 0 : (sm.sel.cM_above + sm.sel.cM_cnt <= kCandCap ? 1 : 2);
       const int ncand = mode == 0 ? total : (mode == 1 ? sm.sel.cM_above + sm.sel.cM_cnt : M);
       SessSync &ss = ws->sync[sess];
       const uint32_t par = sm.epoch & 1u;
@@ -1144,6 +1143,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           const int nhi = sm.sel.nhi;
           const int nwin = min(n_all, k);
           if (nhi <= kDirect) {
+            // per-warp partial counts, in the histogram's words (unused on this path)
+            int *rank_part = reinterpret_cast<int *>(sm.hist);
+            static_assert((kWGThreads / 32) * kDirect <= kHistWords, "rank partials fit the histogram words");
             for (int e0 = 0; e0 < nhi; e0 += kRankStep) {
               unsigned long long x[kRankStep];
               unsigned r[kRankStep];
@@ -1165,13 +1167,13 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
               unsigned mine = 0u;
 #pragma unroll
               for (int j = 0; j < kRankStep; ++j) mine = lane == j ? r[j] : mine;
-              if (lane < kRankStep && e0 + lane < nhi) sm.rank_part[warp][e0 + lane] = int(mine);
+              if (lane < kRankStep && e0 + lane < nhi) rank_part[warp * kDirect + e0 + lane] = int(mine);
             }
             bar512();
             for (int e = tid; e < nhi; e += kWGThreads) {
               int r = 0;
 #pragma unroll
-              for (int w = 0; w < kWGThreads / 32; ++w) r += sm.rank_part[w][e];
+              for (int w = 0; w < kWGThreads / 32; ++w) r += rank_part[w * kDirect + e];
               if (r < k) {
                 const unsigned long long x = sm.sortbuf[e];
                 out_idx[r] = key_index(x);
