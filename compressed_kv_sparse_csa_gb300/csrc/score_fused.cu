@@ -196,6 +196,14 @@ __device__ bool wait_bar(Smem &sm, unsigned long long *bar, uint32_t parity, WsH
   }
 }
 
+// (a0, a1) = (w0 * x0 + a0, w1 * x1 + a1), each rounded once (one packed FMA).
+__device__ __forceinline__ void fma_f32x2(float &a0, float &a1, float w0, float w1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, w, x;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 w, {%2, %3};\n\tmov.b64 x, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, w, x, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
 __device__ __forceinline__ void st_release_shared(int *p, int v) {
   asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
@@ -902,10 +910,10 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
             for (int g = 0; g < 8; ++g) {  // heads 32 half + 4 g .. + 3
               const float4 wv = w4[8 * half + g];
               const uint32_t *v = g < 4 ? v0 + 4 * g : v1 + 4 * (g - 4);
-              acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), acc[0]);
-              acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), acc[1]);
-              acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), acc[2]);
-              acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), acc[3]);
+              fma_f32x2(acc[0], acc[1], wv.x, wv.y, fmaxf(__uint_as_float(v[0]), 0.0f),
+                        fmaxf(__uint_as_float(v[1]), 0.0f));
+              fma_f32x2(acc[2], acc[3], wv.z, wv.w, fmaxf(__uint_as_float(v[2]), 0.0f),
+                        fmaxf(__uint_as_float(v[3]), 0.0f));
             }
           }
           const float s_row = (acc[0] + acc[1]) + (acc[2] + acc[3]);
