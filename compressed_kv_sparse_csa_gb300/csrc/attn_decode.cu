@@ -4,16 +4,16 @@
 // values, 7 UE8M0 scales).  K = V = the dequantised 512-vector, shared by all
 // 64 heads (the indexed attention of the DS4X README, "Nsight Systems").
 //
-// One kernel, no partials in global memory.  The grid is 16 head groups of 4
-// heads, each one cluster of 8 CTAs; CTA s of a cluster takes the selected
-// rows [64 s, 64 s + 64):
+// One kernel, no partials in global memory.  The grid is 64 / HG head groups
+// of HG heads (HG = 4 for one item, 8 for a batch), each one cluster of 8
+// CTAs; CTA s of a cluster takes the selected rows [64 s, 64 s + 64):
 //   1. cp.async gathers each row's bytes (the 16-byte-aligned span holding
 //      the 583-byte row, at most 38 chunks) into that row's slot of shared
 //      memory, all rows at once, so the gather costs one memory round trip;
 //   2. each warp widens its rows in place to fp16: the E4M3 code values
 //      (exact in fp16, |x| <= 448) and the FP16 RoPE values; the block
 //      scales 2^(e-127) go to a small fp32 table;
-//   3. logits for 4 heads x 64 rows on the tensor cores (mma.sync
+//   3. logits for HG heads x 64 rows on the tensor cores (mma.sync
 //      m16n8k16, fp16 operands, fp32 sums; each head's bf16 query scaled
 //      by a power of two into fp16, exact for every value within 2^24 of
 //      the head's largest), each 64-column partial sum scaled by the
@@ -25,9 +25,12 @@
 //      of two);
 //   4. the cluster combines its 8 partials through distributed shared
 //      memory, o_h = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s: each CTA
-//      finishes 1/8 of the group's 4 x 512 outputs, and the LSE M + log L.
-// About 95 KB of shared memory per CTA, so two CTAs fit an SM and all 16
-// clusters are resident at once.
+//      finishes 1/8 of the group's HG x 512 outputs, and the LSE M + log L.
+// About 95 KB (HG = 4) or 98 KB (HG = 8: the partial output reuses the row
+// slots, the logit halves the weight buffer) of shared memory per CTA, so
+// two CTAs fit an SM.  The n = 8 side of every MMA is the group's heads:
+// with HG = 4 half of it is zero rows, with HG = 8 none, so a batch runs
+// half as many CTAs for the same MMA count per CTA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -38,8 +41,6 @@ namespace {
 
 constexpr int kCluster = 8;                         // CTAs per cluster (row splits)
 constexpr int kRows = DS4X_TOPK_MAX / kCluster;     // 64 selected rows per CTA
-constexpr int kHg = 4;                              // heads per cluster
-constexpr int kGroups = DS4X_ATTN_HEADS / kHg;      // 16 clusters
 constexpr int kThreads = 256;
 constexpr int kChunks = 38;                         // 16-byte chunks spanning any 583-byte row
 constexpr int kSlotBytes = 2 * DS4X_KV_DIM + 16;    // 1040: fp16 row + pad (8 rows cover all 32 banks)
@@ -49,21 +50,34 @@ constexpr int kBlocks = DS4X_KV_DIM / DS4X_KV_BLOCK;  // 8: 7 scaled E4M3 blocks
 constexpr int kNopeBlocks = DS4X_KV_NOPE / DS4X_KV_BLOCK;  // 7
 
 // Tensor-core operands (mma.sync m16n8k16, fp16 in, fp32 accumulate): the
-// query as B of the logits (8 rows: 4 heads and 4 zero rows), the softmax
-// weights as B of the output (per 64-column block, 8 rows of 64 weights,
-// as an fp16 pair hi + lo).
+// query as B of the logits (8 rows: the HG heads, then zero rows), the
+// softmax weights as B of the output (per 64-column block, 8 rows of 64
+// weights, as an fp16 pair hi + lo).
 constexpr int kQhStride = 2 * DS4X_KV_DIM + 16;     // 1040 bytes per query row
 constexpr int kPbStride = 2 * kRows + 16;           // 144 bytes per weight row
 constexpr size_t kKhBytes = size_t(kRows) * kSlotBytes;                     // 66,560
 constexpr size_t kQhBytes = size_t(8) * kQhStride;                          // 8,320
 constexpr size_t kPbBytes = size_t(2) * kBlocks * 8 * kPbStride;            // 18,432: hi and lo parts
-constexpr size_t kOpBytes = size_t(kHg) * DS4X_KV_DIM * sizeof(float);      // 8,192: partial output
-constexpr size_t kRedBytes = size_t(2) * kRows * kHg * sizeof(float);       // 2,048: logit halves
-constexpr size_t kSmemBytes = kKhBytes + kQhBytes + kPbBytes + kOpBytes + kRedBytes;
+
+// Per head-group size: HG = 4 keeps the partial output (8 KB) and the logit
+// halves (2 KB) in their own space; HG = 8 puts the partial output (16 KB)
+// over the row slots once the output MMAs are done and the logit halves
+// (4 KB) over the weight buffer before the weights are written.
+template <int HG>
+struct Cfg {
+  static_assert(HG == 4 || HG == 8, "4 or 8 heads per cluster");
+  static constexpr int kGroups = DS4X_ATTN_HEADS / HG;
+  static constexpr bool kShared = HG == 8;
+  static constexpr size_t kOpBytes = size_t(HG) * DS4X_KV_DIM * sizeof(float);
+  static constexpr size_t kRedBytes = size_t(2) * kRows * HG * sizeof(float);
+  static constexpr size_t kSmemBytes =
+      kShared ? kKhBytes + kQhBytes + kPbBytes : kKhBytes + kQhBytes + kPbBytes + kOpBytes + kRedBytes;
+  static_assert(!kShared || (kOpBytes <= kKhBytes && kRedBytes <= kPbBytes), "reused buffers fit");
+};
 static_assert(kRows * kCluster == DS4X_TOPK_MAX, "clusters cover the maximum k");
 static_assert(kChunks * 16 <= kSlotBytes && kSlotBytes % 16 == 0, "a row's bytes fit its slot");
-static_assert(kHg * DS4X_KV_DIM == kThreads * 8, "one 16-byte query load per thread");
-static_assert(kHg * DS4X_KV_DIM == kCluster * kThreads, "one combined output per thread");
+static_assert(4 * DS4X_KV_DIM == kThreads * 8, "one 16-byte query load per thread per 4 heads");
+static_assert(4 * DS4X_KV_DIM == kCluster * kThreads, "one combined output per thread per 4 heads");
 static_assert(kThreads / 32 == kBlocks && kRows == 4 * 16, "warp w: output block w; logits: 4 row tiles x 2 block halves");
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
@@ -141,8 +155,11 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
   return v;
 }
 
+template <int HG>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
 attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
+  using C = Cfg<HG>;
+  constexpr int kQLoads = HG / 4;  // 16-byte query loads (and combined outputs) per thread
   // batch item blockIdx.z: its cache, selected rows, query and output
   const int bz = blockIdx.z;
   const uint8_t *__restrict__ kv = ab.kv_arr != nullptr ? ab.kv_arr[bz] : ab.kv;
@@ -157,26 +174,30 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
   unsigned char *Qh = smem + kKhBytes;                        // [8][1040]: scaled query, fp16
   unsigned char *Pb = Qh + kQhBytes;                          // [hi, lo][8 blocks][8][144]: weights, fp16
-  float *Opart = reinterpret_cast<float *>(Pb + kPbBytes);    // [4][512]
-  float *red = Opart + kHg * DS4X_KV_DIM;                     // [2][64][4]
-  __shared__ __align__(16) float Pt[kRows][kHg];   // logits, then exp(l - m)
+  float *Opart = C::kShared ? reinterpret_cast<float *>(Kh)                 // [HG][512]
+                            : reinterpret_cast<float *>(Pb + kPbBytes);
+  float *red = C::kShared ? reinterpret_cast<float *>(Pb) : Opart + HG * DS4X_KV_DIM;  // [2][64][HG]
+  __shared__ __align__(16) float Pt[kRows][HG];    // logits, then exp(l - m)
   __shared__ float sc[kRows][kBlocks];             // block scales (1 for the RoPE tail)
-  __shared__ float ml[2 * kHg];                    // m[4], l[4] of this split
-  __shared__ float qmax[kThreads / 32];            // per warp: largest |q| of its head
+  __shared__ float ml[2 * HG];                     // m[HG], l[HG] of this split
+  __shared__ float qmax[kQLoads][kThreads / 32];   // per load and warp: largest |q| of its head
   __shared__ float sbmax[kBlocks];                 // per block: largest row scale
-  __shared__ float fw[kHg][kCluster];              // combine weights e^(m_s - M) per head and split
-  __shared__ float fl[kHg];                        // ... and their sum L per head
+  __shared__ float fw[HG][kCluster];               // combine weights e^(m_s - M) per head and split
+  __shared__ float fl[HG];                         // ... and their sum L per head
   __shared__ int64_t rows_s[kRows];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, hg = blockIdx.y;
 
-  // the zero rows 4..7 of the query operand and of every weight block
-  for (int i = tid; i < 4 * kQhStride / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(Qh + 4 * kQhStride)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = tid; i < 2 * kBlocks * 4 * kPbStride / 16; i += kThreads) {
-    const int blk = i / (4 * kPbStride / 16), j = i % (4 * kPbStride / 16);  // blk: part * 8 + block
-    reinterpret_cast<uint4 *>(Pb + blk * 8 * kPbStride + 4 * kPbStride)[j] = make_uint4(0u, 0u, 0u, 0u);
+  // the zero rows HG..7 of the query operand and of every weight block
+  if (HG < 8) {
+    constexpr int kZero = (HG < 8 ? 8 - HG : 1) * kPbStride / 16;  // 16-byte words of a block's zero rows
+    for (int i = tid; i < (8 - HG) * kQhStride / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(Qh + HG * kQhStride)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < 2 * kBlocks * kZero; i += kThreads) {
+      const int blk = i / kZero, j = i % kZero;  // blk: part * 8 + block
+      reinterpret_cast<uint4 *>(Pb + blk * 8 * kPbStride + HG * kPbStride)[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   // Launched as a programmatic dependent of the previous kernel (the scorer
   // that wrote idx): everything above reads no input; wait for it here.
@@ -193,23 +214,26 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
     rows_s[tid] = r;
   }
-  // query: thread t holds 8 values of head t / 64 (two warps per head)
-  float qv[8];
-  {
-    const uint4 qb = reinterpret_cast<const uint4 *>(q + size_t(hg) * kHg * DS4X_KV_DIM)[tid];
+  // query: load j of thread t holds 8 values of head 4 j + t / 64 (two warps per head)
+  float qv[kQLoads][8];
+#pragma unroll
+  for (int j = 0; j < kQLoads; ++j) {
+    const uint4 qb = reinterpret_cast<const uint4 *>(q + size_t(hg) * HG * DS4X_KV_DIM)[j * kThreads + tid];
     const uint32_t w[4] = {qb.x, qb.y, qb.z, qb.w};
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      qv[2 * i] = __uint_as_float(w[i] << 16);
-      qv[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      m = fmaxf(m, fmaxf(fabsf(qv[2 * i]), fabsf(qv[2 * i + 1])));
+      qv[j][2 * i] = __uint_as_float(w[i] << 16);
+      qv[j][2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      m = fmaxf(m, fmaxf(fabsf(qv[j][2 * i]), fabsf(qv[j][2 * i + 1])));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) qmax[warp] = m;
+    if (lane == 0) qmax[j][warp] = m;
   }
   __syncthreads();
+  // head h's largest |q|: load h / 4, warps 2 (h % 4) and 2 (h % 4) + 1
+  auto head_qmax = [&](int h) { return fmaxf(qmax[h >> 2][2 * (h & 3)], qmax[h >> 2][2 * (h & 3) + 1]); };
 
   // 1. gather: chunk c of row rr is bytes [a0 + 16 c, a0 + 16 c + 16), a0 the
   // row's start rounded down to 16; chunks past the row's end are skipped and
@@ -233,12 +257,13 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   // while the rows are in flight: head h's query scaled by 2^e_h so that its
   // largest value lies in [2^14, 2^15): every bf16 value in that range is
   // exact in fp16, and the logits are scaled back by 2^-e_h (exactly)
-  {
-    const int hq = tid >> 6;
-    const float s = pow2f(query_exp(fmaxf(qmax[2 * hq], qmax[2 * hq + 1])));
+#pragma unroll
+  for (int j = 0; j < kQLoads; ++j) {
+    const int hq = 4 * j + (tid >> 6);
+    const float s = pow2f(query_exp(head_qmax(hq)));
     __half hv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(qv[i] * s);
+    for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(qv[j][i] * s);
     *reinterpret_cast<uint4 *>(Qh + hq * kQhStride + 16 * (tid & 63)) = *reinterpret_cast<const uint4 *>(hv);
   }
   cp_async_wait_all();
@@ -303,7 +328,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   // 3a. logits on the tensor cores: warp w takes rows 16 (w % 4) .. + 16 and
   // blocks 4 (w / 4) .. + 4; each block's 64-column partial sum is scaled by
   // the row's block scale.  C fragment: rows g and g + 8 (g = lane / 4),
-  // heads 2 (lane % 4) and + 1 (heads 4..7 are the zero rows).
+  // heads 2 (lane % 4) and + 1 (heads HG..7 are the zero rows).
   {
     const int mt = warp & 3, bh = warp >> 2, g = lane >> 2, hc = 2 * (lane & 3);
     const int r0 = 16 * mt + g, r1 = r0 + 8;
@@ -328,26 +353,27 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       tot[2] = fmaf(s1, acc[2], tot[2]);
       tot[3] = fmaf(s1, acc[3], tot[3]);
     }
-    if (hc < kHg) {
-      float *rb = red + bh * kRows * kHg;
-      rb[r0 * kHg + hc] = tot[0];
-      rb[r0 * kHg + hc + 1] = tot[1];
-      rb[r1 * kHg + hc] = tot[2];
-      rb[r1 * kHg + hc + 1] = tot[3];
+    if (hc < HG) {
+      float *rb = red + bh * kRows * HG;
+      rb[r0 * HG + hc] = tot[0];
+      rb[r0 * HG + hc + 1] = tot[1];
+      rb[r1 * HG + hc] = tot[2];
+      rb[r1 * HG + hc + 1] = tot[3];
     }
   }
   __syncthreads();
-  if (tid < kRows * kHg) {
-    const int r = tid / kHg, h = tid % kHg;
-    const float unscale = pow2f(-query_exp(fmaxf(qmax[2 * h], qmax[2 * h + 1])));
-    const float l = (red[r * kHg + h] + red[kRows * kHg + r * kHg + h]) * unscale;
+  for (int e = tid; e < kRows * HG; e += kThreads) {
+    const int r = e / HG, h = e % HG;
+    const float unscale = pow2f(-query_exp(head_qmax(h)));
+    const float l = (red[r * HG + h] + red[kRows * HG + r * HG + h]) * unscale;
     Pt[r][h] = rows_s[r] >= 0 ? l * scale : -INFINITY;
   }
   __syncthreads();
 
-  // 3b. split softmax statistics: warp h < 4 takes head h, rows lane, lane + 32;
-  // warps 4..7 find each block's largest row scale.
-  if (warp < kHg) {
+  // 3b. split softmax statistics: warp h < HG takes head h, rows lane, lane + 32;
+  // the other warps (every warp, for HG = 8, after its head) find each
+  // block's largest row scale.
+  if (warp < HG) {
     const int h = warp;
     const float l0 = Pt[lane][h], l1 = Pt[lane + 32][h];
     float m = fmaxf(l0, l1);
@@ -362,12 +388,14 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) {
       ml[h] = m;
-      ml[kHg + h] = s;
+      ml[HG + h] = s;
     }
-  } else {
+  }
+  if (HG == 8 || warp >= HG) {
+    constexpr int kPer = kBlocks / (kThreads / 32 - (HG == 8 ? 0 : HG));  // blocks per warp: 1 or 2
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int blk = 2 * (warp - kHg) + j;
+    for (int j = 0; j < kPer; ++j) {
+      const int blk = kPer * (HG == 8 ? warp : warp - HG) + j;
       float m = fmaxf(sc[lane][blk], sc[lane + 32][blk]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -378,8 +406,8 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   // 3c. output weights per block: exp(l - m) times the row's block scale over
   // the block's largest (a power of two at most 1, exact), as fp16 hi + lo
   // (hi the rounded weight, lo the rounded remainder: 22 significant bits)
-  for (int e = tid; e < kBlocks * kHg * kRows; e += kThreads) {
-    const int blk = e / (kHg * kRows), h = (e / kRows) % kHg, r = e % kRows;
+  for (int e = tid; e < kBlocks * HG * kRows; e += kThreads) {
+    const int blk = e / (HG * kRows), h = (e / kRows) % HG, r = e % kRows;
     const float smax = sbmax[blk];
     const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] / smax) : 0.f;
     const __half hi = __float2half_rn(w);
@@ -416,7 +444,8 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       }
     }
     const float smax = sbmax[blk];
-    if (hc < kHg) {
+    if (C::kShared) __syncthreads();  // the partial output goes over the row slots the other warps read
+    if (hc < HG) {
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int d0 = DS4X_KV_BLOCK * blk + 16 * t + g;
@@ -433,10 +462,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   // f_s = e^(m_s - M), the sum L = sum_s f_s l_s and the LSE; then every
   // thread reads its 8 partial outputs and divides sum_s f_s o_s by L.
   cluster_sync();
-  if (warp == 0) {
-    // lane = split s (8) x head h (4)
-    const int s = lane & (kCluster - 1), h = lane >> 3;
-    const float ms = ld_peer(&ml[h], uint32_t(s)), ls = ld_peer(&ml[kHg + h], uint32_t(s));
+  if (warp < HG / 4) {
+    // lane = split s (8) x head h (4 per warp)
+    const int s = lane & (kCluster - 1), h = 4 * warp + (lane >> 3);
+    const float ms = ld_peer(&ml[h], uint32_t(s)), ls = ld_peer(&ml[HG + h], uint32_t(s));
     float M = ms;
 #pragma unroll
     for (int o = 1; o < kCluster; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -446,11 +475,12 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     for (int o = 1; o < kCluster; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     fw[h][s] = f;
     if (s == 0) fl[h] = L;
-    if (s == 0 && lse != nullptr && cluster_rank() == 0) lse[hg * kHg + h] = L > 0.f ? M + logf(L) : -INFINITY;
+    if (s == 0 && lse != nullptr && cluster_rank() == 0) lse[hg * HG + h] = L > 0.f ? M + logf(L) : -INFINITY;
   }
   __syncthreads();
-  {
-    const int e = int(cluster_rank()) * kThreads + tid;
+#pragma unroll
+  for (int j = 0; j < kQLoads; ++j) {
+    const int e = int(cluster_rank()) * kQLoads * kThreads + j * kThreads + tid;
     const int h = e / DS4X_KV_DIM, d = e % DS4X_KV_DIM;
     float os[kCluster];
 #pragma unroll
@@ -459,7 +489,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 #pragma unroll
     for (int s = 0; s < kCluster; ++s) o = fmaf(fw[h][s], os[s], o);
     const float L = fl[h];
-    out[size_t(hg * kHg + h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+    out[size_t(hg * HG + h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
   }
   cluster_wait_peers();  // peers may still be reading this CTA's partials
 }
@@ -468,24 +498,38 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 
 size_t attn_decode_ws_bytes(int32_t) { return kWsHeaderBytes; }
 
-cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+template <int HG>
+cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+  using C = Cfg<HG>;
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = set_max_smem_once(attn_decode_kernel, int(kSmemBytes), smem_set);
+  cudaError_t e = set_max_smem_once(attn_decode_kernel<HG>, int(C::kSmemBytes), smem_set);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the CTAs may start while the previous
   // kernel finishes (it lets them go from its tail); the kernel waits for it
   // before reading anything.
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kCluster, kGroups, unsigned(batch));
+  cfg.gridDim = dim3(kCluster, C::kGroups, unsigned(batch));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, ab, static_cast<WsHeader *>(ws));
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<HG>, ab, static_cast<WsHeader *>(ws));
+}
+
+cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+  // 4 heads per cluster while the grid fits one wave (two CTAs per SM): the
+  // most CTAs, the shortest latency; beyond that 8, half the CTAs for the
+  // same MMA count each (no zero rows)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas4 = int64_t(batch) * kCluster * Cfg<4>::kGroups;
+  return ctas4 <= 2 * int64_t(sms) ? launch_attn_hg<4>(ab, batch, ws, stream) : launch_attn_hg<8>(ab, batch, ws, stream);
 }
 
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

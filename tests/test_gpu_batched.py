@@ -113,3 +113,33 @@ def test_prefill_attention_per_query():
         ref_out, _, ref_lse = A.sparse_attn_decode(packed, idx[i], case["q_attn"][i], SOFTMAX_SCALE)
         check_attention(got[i], ref_out)
         np.testing.assert_allclose(got_lse[i], ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("k", [512, 333])
+def test_batched_attention_equals_single(k):
+    """A batch runs 8 heads per cluster, one item 4: the per-head arithmetic
+    is the same, so each session's output and LSE agree bit for bit."""
+    B = require_gpu()
+    sess = sessions_case(n_sess=3, scale_lengths=0.02)
+    _, kv_rows = _pack_sessions(sess)
+    n = torch.tensor([s["n"] for s in sess], dtype=torch.int64, device="cuda")
+    rng = np.random.default_rng(11)
+    idx = np.full((3, k), -1, dtype=np.int32)  # sessions shorter than k: ragged lists
+    for j, s in enumerate(sess):
+        m = min(k, s["n"])
+        idx[j, :m] = rng.choice(s["n"], size=m, replace=False)
+    idx[1, k // 2:] = -1
+    q = np.stack([s["q_attn"] for s in sess])
+    ws = new_ws(B.ds4x_sparse_attn_decode_workspace(k))
+    out_b = torch.empty((3, 64, 512), dtype=torch.bfloat16, device="cuda")
+    lse_b = torch.empty((3, 64), dtype=torch.float32, device="cuda")
+    B.ds4x_sparse_attn_decode_batched(_ptrs(kv_rows), n, dev(idx), k, bf16_dev(q), SOFTMAX_SCALE, out_b, lse_b, ws)
+    for j, s in enumerate(sess):
+        out_1 = torch.empty((64, 512), dtype=torch.bfloat16, device="cuda")
+        lse_1 = torch.empty(64, dtype=torch.float32, device="cuda")
+        B.ds4x_sparse_attn_decode(kv_rows[j], s["n"], dev(idx[j]), k, bf16_dev(s["q_attn"]), SOFTMAX_SCALE, out_1,
+                                  lse_1, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out_1.view(torch.int16), out_b[j].view(torch.int16)), j
+        assert torch.equal(lse_1.view(torch.int32), lse_b[j].view(torch.int32)), j
+    assert B.ds4x_workspace_status(ws) == 0
