@@ -5,8 +5,9 @@
 // 64 heads (the indexed attention of the DS4X README, "Nsight Systems").
 //
 // One kernel, no partials in global memory.  The grid is 64 / HG head groups
-// of HG heads (HG = 4 for one item, 8 for a batch), each one cluster of 8
-// CTAs; CTA s of a cluster takes the selected rows [64 s, 64 s + 64):
+// of HG heads (HG = 4, 8 or 16: the fewest heads whose grid fits one
+// resident wave, else 16), each one cluster of 8 CTAs; CTA s of a cluster
+// takes the selected rows [64 s, 64 s + 64):
 //   1. cp.async gathers each row's bytes (the 16-byte-aligned span holding
 //      the 583-byte row, at most 38 chunks) into that row's slot of shared
 //      memory, all rows at once, so the gather costs one memory round trip;
@@ -26,11 +27,11 @@
 //   4. the cluster combines its 8 partials through distributed shared
 //      memory, o_h = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s: each CTA
 //      finishes 1/8 of the group's HG x 512 outputs, and the LSE M + log L.
-// About 95 KB (HG = 4) or 98 KB (HG = 8: the partial output reuses the row
-// slots, the logit halves the weight buffer) of shared memory per CTA, so
-// two CTAs fit an SM.  The n = 8 side of every MMA is the group's heads:
-// with HG = 4 half of it is zero rows, with HG = 8 none, so a batch runs
-// half as many CTAs for the same MMA count per CTA.
+// About 95 KB (HG = 4), 98 KB (HG = 8) or 107 KB (HG = 16) of shared memory
+// per CTA, so two CTAs fit an SM: from HG = 8 on, the partial output reuses
+// the row slots and the logit halves the weight buffer, and HG = 16 makes
+// its weights and output MMAs in two passes of 8 heads.  The n = 8 side of
+// every MMA is 8 of the group's heads: with HG = 4 half of it is zero rows.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -56,22 +57,25 @@ constexpr int kNopeBlocks = DS4X_KV_NOPE / DS4X_KV_BLOCK;  // 7
 constexpr int kQhStride = 2 * DS4X_KV_DIM + 16;     // 1040 bytes per query row
 constexpr int kPbStride = 2 * kRows + 16;           // 144 bytes per weight row
 constexpr size_t kKhBytes = size_t(kRows) * kSlotBytes;                     // 66,560
-constexpr size_t kQhBytes = size_t(8) * kQhStride;                          // 8,320
 constexpr size_t kPbBytes = size_t(2) * kBlocks * 8 * kPbStride;            // 18,432: hi and lo parts
 
 // Per head-group size: HG = 4 keeps the partial output (8 KB) and the logit
-// halves (2 KB) in their own space; HG = 8 puts the partial output (16 KB)
-// over the row slots once the output MMAs are done and the logit halves
-// (4 KB) over the weight buffer before the weights are written.
+// halves (2 KB) in their own space; HG >= 8 puts the partial output (16 or
+// 32 KB) over the row slots once the output MMAs are done and the logit
+// halves (4 or 8 KB) over the weight buffer before the weights are written.
 template <int HG>
 struct Cfg {
-  static_assert(HG == 4 || HG == 8, "4 or 8 heads per cluster");
+  static_assert(HG == 4 || HG == 8 || HG == 16, "4, 8 or 16 heads per cluster");
   static constexpr int kGroups = DS4X_ATTN_HEADS / HG;
-  static constexpr bool kShared = HG == 8;
+  static constexpr bool kShared = HG >= 8;
+  static constexpr int kNT = HG > 8 ? HG / 8 : 1;  // 8-head n tiles of the logits, passes of the output
+  static constexpr int kPH = HG > 8 ? 8 : HG;      // heads per output pass
+  static constexpr size_t kQhBytes = size_t(8 * kNT) * kQhStride;  // query rows: the heads, then zero rows
   static constexpr size_t kOpBytes = size_t(HG) * DS4X_KV_DIM * sizeof(float);
   static constexpr size_t kRedBytes = size_t(2) * kRows * HG * sizeof(float);
   static constexpr size_t kSmemBytes =
       kShared ? kKhBytes + kQhBytes + kPbBytes : kKhBytes + kQhBytes + kPbBytes + kOpBytes + kRedBytes;
+  static_assert(kSmemBytes + 8 * 1024 <= 113 * 1024, "two CTAs per SM (with up to 8 KB of static shared memory)");
   static_assert(!kShared || (kOpBytes <= kKhBytes && kRedBytes <= kPbBytes), "reused buffers fit");
 };
 static_assert(kRows * kCluster == DS4X_TOPK_MAX, "clusters cover the maximum k");
@@ -173,7 +177,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
   unsigned char *Qh = smem + kKhBytes;                        // [8][1040]: scaled query, fp16
-  unsigned char *Pb = Qh + kQhBytes;                          // [hi, lo][8 blocks][8][144]: weights, fp16
+  unsigned char *Pb = Qh + C::kQhBytes;                       // [hi, lo][8 blocks][8][144]: weights, fp16
   float *Opart = C::kShared ? reinterpret_cast<float *>(Kh)                 // [HG][512]
                             : reinterpret_cast<float *>(Pb + kPbBytes);
   float *red = C::kShared ? reinterpret_cast<float *>(Pb) : Opart + HG * DS4X_KV_DIM;  // [2][64][HG]
@@ -328,37 +332,57 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   // 3a. logits on the tensor cores: warp w takes rows 16 (w % 4) .. + 16 and
   // blocks 4 (w / 4) .. + 4; each block's 64-column partial sum is scaled by
   // the row's block scale.  C fragment: rows g and g + 8 (g = lane / 4),
-  // heads 2 (lane % 4) and + 1 (heads HG..7 are the zero rows).
+  // heads 8 n + 2 (lane % 4) and + 1 of n tile n (heads HG..7 are the zero
+  // rows); each key fragment serves every n tile.
   {
     const int mt = warp & 3, bh = warp >> 2, g = lane >> 2, hc = 2 * (lane & 3);
     const int r0 = 16 * mt + g, r1 = r0 + 8;
     const unsigned char *a_base = Kh + (16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8) * kSlotBytes + ((lane >> 4) & 1) * 16;
     const unsigned char *b_base = Qh + (lane & 7) * kQhStride + ((lane >> 3) & 1) * 16;
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
+    float tot[C::kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::kNT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tot[nt][j] = 0.f;
 #pragma unroll
     for (int bi = 0; bi < 4; ++bi) {
       const int blk = 4 * bh + bi;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[C::kNT][4];
+#pragma unroll
+      for (int nt = 0; nt < C::kNT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const int k0 = DS4X_KV_BLOCK * blk + 16 * ks;  // columns k0 .. k0 + 15
-        uint32_t af[4], bf[2];
+        uint32_t af[4];
         ldsm_x4(a_base + 2 * k0, af);
-        ldsm_x2(b_base + 2 * k0, bf);
-        mma_16816(acc, af, bf);
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+          uint32_t bf[2];
+          ldsm_x2(b_base + 8 * nt * kQhStride + 2 * k0, bf);
+          mma_16816(acc[nt], af, bf);
+        }
       }
       const float s0 = sc[r0][blk], s1 = sc[r1][blk];
-      tot[0] = fmaf(s0, acc[0], tot[0]);
-      tot[1] = fmaf(s0, acc[1], tot[1]);
-      tot[2] = fmaf(s1, acc[2], tot[2]);
-      tot[3] = fmaf(s1, acc[3], tot[3]);
+#pragma unroll
+      for (int nt = 0; nt < C::kNT; ++nt) {
+        tot[nt][0] = fmaf(s0, acc[nt][0], tot[nt][0]);
+        tot[nt][1] = fmaf(s0, acc[nt][1], tot[nt][1]);
+        tot[nt][2] = fmaf(s1, acc[nt][2], tot[nt][2]);
+        tot[nt][3] = fmaf(s1, acc[nt][3], tot[nt][3]);
+      }
     }
-    if (hc < HG) {
-      float *rb = red + bh * kRows * HG;
-      rb[r0 * HG + hc] = tot[0];
-      rb[r0 * HG + hc + 1] = tot[1];
-      rb[r1 * HG + hc] = tot[2];
-      rb[r1 * HG + hc + 1] = tot[3];
+    float *rb = red + bh * kRows * HG;
+#pragma unroll
+    for (int nt = 0; nt < C::kNT; ++nt) {
+      const int h = 8 * nt + hc;
+      if (h < HG) {
+        rb[r0 * HG + h] = tot[nt][0];
+        rb[r0 * HG + h + 1] = tot[nt][1];
+        rb[r1 * HG + h] = tot[nt][2];
+        rb[r1 * HG + h + 1] = tot[nt][3];
+      }
     }
   }
   __syncthreads();
@@ -370,11 +394,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   }
   __syncthreads();
 
-  // 3b. split softmax statistics: warp h < HG takes head h, rows lane, lane + 32;
-  // the other warps (every warp, for HG = 8, after its head) find each
-  // block's largest row scale.
-  if (warp < HG) {
-    const int h = warp;
+  // 3b. split softmax statistics: warp w takes heads w, w + 8, ... (< HG),
+  // rows lane, lane + 32; the warps without a head (every warp, for HG >= 8,
+  // after its heads) find each block's largest row scale.
+  for (int h = warp; h < HG; h += kThreads / 32) {
     const float l0 = Pt[lane][h], l1 = Pt[lane + 32][h];
     float m = fmaxf(l0, l1);
 #pragma unroll
@@ -391,11 +414,11 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       ml[HG + h] = s;
     }
   }
-  if (HG == 8 || warp >= HG) {
-    constexpr int kPer = kBlocks / (kThreads / 32 - (HG == 8 ? 0 : HG));  // blocks per warp: 1 or 2
+  if (HG >= 8 || warp >= HG) {
+    constexpr int kPer = kBlocks / (kThreads / 32 - (HG >= 8 ? 0 : HG));  // blocks per warp: 1 or 2
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int blk = kPer * (HG == 8 ? warp : warp - HG) + j;
+      const int blk = kPer * (HG >= 8 ? warp : warp - HG) + j;
       float m = fmaxf(sc[lane][blk], sc[lane + 32][blk]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -403,30 +426,35 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
   }
   __syncthreads();
+  // 3c/3d, per pass of up to 8 heads (HG = 16: two passes over one weight
+  // buffer; the accumulators stay in registers until the row slots are done).
   // 3c. output weights per block: exp(l - m) times the row's block scale over
   // the block's largest (a power of two at most 1, exact), as fp16 hi + lo
-  // (hi the rounded weight, lo the rounded remainder: 22 significant bits)
-  for (int e = tid; e < kBlocks * HG * kRows; e += kThreads) {
-    const int blk = e / (HG * kRows), h = (e / kRows) % HG, r = e % kRows;
-    const float smax = sbmax[blk];
-    const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] / smax) : 0.f;
-    const __half hi = __float2half_rn(w);
-    const __half lo = __float2half_rn(w - __half2float(hi));
-    reinterpret_cast<__half *>(Pb + (blk * 8 + h) * kPbStride)[r] = hi;
-    reinterpret_cast<__half *>(Pb + ((kBlocks + blk) * 8 + h) * kPbStride)[r] = lo;
-  }
-  __syncthreads();
-
+  // (hi the rounded weight, lo the rounded remainder: 22 significant bits).
   // 3d. partial output on the tensor cores: warp w takes block w (columns
   // 64 w .. + 64, four 16-column tiles); A = the rows' values transposed, B =
   // the block's weights; the block's largest scale goes back on at the end.
-  {
-    const int blk = warp, g = lane >> 2, hc = 2 * (lane & 3);
-    float acc[4][4];
+  const int g = lane >> 2, hc = 2 * (lane & 3);
+  float acc[C::kNT][4][4];
+#pragma unroll
+  for (int pass = 0; pass < C::kNT; ++pass) {
+    if (pass > 0) __syncthreads();  // the previous pass's MMAs have read the weights
+    for (int e = tid; e < kBlocks * C::kPH * kRows; e += kThreads) {
+      const int blk = e / (C::kPH * kRows), hl = (e / kRows) % C::kPH, r = e % kRows;
+      const int h = C::kPH * pass + hl;
+      const float smax = sbmax[blk];
+      const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] / smax) : 0.f;
+      const __half hi = __float2half_rn(w);
+      const __half lo = __float2half_rn(w - __half2float(hi));
+      reinterpret_cast<__half *>(Pb + (blk * 8 + hl) * kPbStride)[r] = hi;
+      reinterpret_cast<__half *>(Pb + ((kBlocks + blk) * 8 + hl) * kPbStride)[r] = lo;
+    }
+    __syncthreads();
+    const int blk = warp;
 #pragma unroll
     for (int t = 0; t < 4; ++t)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[t][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[pass][t][j] = 0.f;
     const unsigned char *pb = Pb + blk * 8 * kPbStride + (lane & 7) * kPbStride + ((lane >> 3) & 1) * 16;
 #pragma unroll
     for (int ks = 0; ks < kRows / 16; ++ks) {
@@ -439,20 +467,27 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       for (int t = 0; t < 4; ++t) {
         uint32_t af[4];
         ldsm_x4_trans(a_base + 2 * (DS4X_KV_BLOCK * blk + 16 * t), af);
-        mma_16816(acc[t], af, bh);
-        mma_16816(acc[t], af, bl);
+        mma_16816(acc[pass][t], af, bh);
+        mma_16816(acc[pass][t], af, bl);
       }
     }
+  }
+  {
+    const int blk = warp;
     const float smax = sbmax[blk];
     if (C::kShared) __syncthreads();  // the partial output goes over the row slots the other warps read
-    if (hc < HG) {
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int d0 = DS4X_KV_BLOCK * blk + 16 * t + g;
-        Opart[hc * DS4X_KV_DIM + d0] = acc[t][0] * smax;
-        Opart[(hc + 1) * DS4X_KV_DIM + d0] = acc[t][1] * smax;
-        Opart[hc * DS4X_KV_DIM + d0 + 8] = acc[t][2] * smax;
-        Opart[(hc + 1) * DS4X_KV_DIM + d0 + 8] = acc[t][3] * smax;
+    for (int pass = 0; pass < C::kNT; ++pass) {
+      const int h = C::kPH * pass + hc;
+      if (hc < C::kPH) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int d0 = DS4X_KV_BLOCK * blk + 16 * t + g;
+          Opart[h * DS4X_KV_DIM + d0] = acc[pass][t][0] * smax;
+          Opart[(h + 1) * DS4X_KV_DIM + d0] = acc[pass][t][1] * smax;
+          Opart[h * DS4X_KV_DIM + d0 + 8] = acc[pass][t][2] * smax;
+          Opart[(h + 1) * DS4X_KV_DIM + d0 + 8] = acc[pass][t][3] * smax;
+        }
       }
     }
   }
@@ -521,15 +556,17 @@ cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_
 }
 
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
-  // 4 heads per cluster while the grid fits one wave (two CTAs per SM): the
-  // most CTAs, the shortest latency; beyond that 8, half the CTAs for the
-  // same MMA count each (no zero rows)
+  // the fewest heads per cluster whose grid fits one wave (two CTAs per SM):
+  // the most CTAs, the shortest latency; beyond that 16, a quarter of the
+  // CTAs of 4 heads for about twice the MMAs each (no zero rows)
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int64_t ctas4 = int64_t(batch) * kCluster * Cfg<4>::kGroups;
-  return ctas4 <= 2 * int64_t(sms) ? launch_attn_hg<4>(ab, batch, ws, stream) : launch_attn_hg<8>(ab, batch, ws, stream);
+  const int64_t wave = 2 * int64_t(sms);
+  if (int64_t(batch) * kCluster * Cfg<4>::kGroups <= wave) return launch_attn_hg<4>(ab, batch, ws, stream);
+  if (int64_t(batch) * kCluster * Cfg<8>::kGroups <= wave) return launch_attn_hg<8>(ab, batch, ws, stream);
+  return launch_attn_hg<16>(ab, batch, ws, stream);
 }
 
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

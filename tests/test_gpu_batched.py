@@ -115,24 +115,26 @@ def test_prefill_attention_per_query():
         np.testing.assert_allclose(got_lse[i], ref_lse, rtol=1e-5, atol=1e-5)
 
 
-@pytest.mark.parametrize("k", [512, 333])
-def test_batched_attention_equals_single(k):
-    """A batch runs 8 heads per cluster, one item 4: the per-head arithmetic
-    is the same, so each session's output and LSE agree bit for bit."""
+@pytest.mark.parametrize("n_sess,k", [(3, 512), (3, 333), (6, 512)])
+def test_batched_attention_equals_single(n_sess, k):
+    """One item runs 4 heads per cluster, a batch 8 or 16 (the fewest whose
+    grid fits one wave of 2 CTAs per SM, else 16: 3 sessions take 8 and 6
+    take 16 on 152 SMs): the per-head arithmetic is the same, so each
+    session's output and LSE agree bit for bit."""
     B = require_gpu()
-    sess = sessions_case(n_sess=3, scale_lengths=0.02)
+    sess = sessions_case(n_sess=n_sess, scale_lengths=0.02)
     _, kv_rows = _pack_sessions(sess)
     n = torch.tensor([s["n"] for s in sess], dtype=torch.int64, device="cuda")
     rng = np.random.default_rng(11)
-    idx = np.full((3, k), -1, dtype=np.int32)  # sessions shorter than k: ragged lists
+    idx = np.full((n_sess, k), -1, dtype=np.int32)  # sessions shorter than k: ragged lists
     for j, s in enumerate(sess):
         m = min(k, s["n"])
         idx[j, :m] = rng.choice(s["n"], size=m, replace=False)
     idx[1, k // 2:] = -1
     q = np.stack([s["q_attn"] for s in sess])
     ws = new_ws(B.ds4x_sparse_attn_decode_workspace(k))
-    out_b = torch.empty((3, 64, 512), dtype=torch.bfloat16, device="cuda")
-    lse_b = torch.empty((3, 64), dtype=torch.float32, device="cuda")
+    out_b = torch.empty((n_sess, 64, 512), dtype=torch.bfloat16, device="cuda")
+    lse_b = torch.empty((n_sess, 64), dtype=torch.float32, device="cuda")
     B.ds4x_sparse_attn_decode_batched(_ptrs(kv_rows), n, dev(idx), k, bf16_dev(q), SOFTMAX_SCALE, out_b, lse_b, ws)
     for j, s in enumerate(sess):
         out_1 = torch.empty((64, 512), dtype=torch.bfloat16, device="cuda")
