@@ -151,6 +151,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 // Loads a float from the same shared-memory offset in cluster CTA `rank`.
+// Loads N consecutive floats (16-byte aligned for N = 4, 8 for N = 2) from
+// the same shared-memory offset in cluster CTA `rank`.
+template <int N>
+__device__ __forceinline__ void ld_peer_vec(const float *local, uint32_t rank, float (&v)[N]) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  if constexpr (N == 4) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(ra));
+  } else if constexpr (N == 2) {
+    asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(ra));
+  } else {
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v[0]) : "r"(ra));
+  }
+}
 __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
   uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
   float v;
@@ -181,11 +196,13 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   float *Opart = C::kShared ? reinterpret_cast<float *>(Kh)                 // [HG][512]
                             : reinterpret_cast<float *>(Pb + kPbBytes);
   float *red = C::kShared ? reinterpret_cast<float *>(Pb) : Opart + HG * DS4X_KV_DIM;  // [2][64][HG]
-  __shared__ __align__(16) float Pt[kRows][HG];    // logits, then exp(l - m)
-  __shared__ float sc[kRows][kBlocks];             // block scales (1 for the RoPE tail)
+  // odd row strides: a warp reading one column over 32 rows hits 32 banks
+  __shared__ float Pt[kRows][HG + 1];              // logits, then exp(l - m)
+  __shared__ float sc[kRows][kBlocks + 1];         // block scales (1 for the RoPE tail)
   __shared__ float ml[2 * HG];                     // m[HG], l[HG] of this split
   __shared__ float qmax[kQLoads][kThreads / 32];   // per load and warp: largest |q| of its head
   __shared__ float sbmax[kBlocks];                 // per block: largest row scale
+  __shared__ float sbinv[kBlocks];                 // ... and its reciprocal (exact: a power of two)
   __shared__ float fw[HG][kCluster];               // combine weights e^(m_s - M) per head and split
   __shared__ float fl[HG];                         // ... and their sum L per head
   __shared__ int64_t rows_s[kRows];
@@ -422,7 +439,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       float m = fmaxf(sc[lane][blk], sc[lane + 32][blk]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sbmax[blk] = m;
+      if (lane == 0) {
+        sbmax[blk] = m;
+        sbinv[blk] = m > 0.f ? 1.0f / m : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -443,7 +463,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       const int blk = e / (C::kPH * kRows), hl = (e / kRows) % C::kPH, r = e % kRows;
       const int h = C::kPH * pass + hl;
       const float smax = sbmax[blk];
-      const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] / smax) : 0.f;
+      const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] * sbinv[blk]) : 0.f;  // the ratio is exact
       const __half hi = __float2half_rn(w);
       const __half lo = __float2half_rn(w - __half2float(hi));
       reinterpret_cast<__half *>(Pb + (blk * 8 + hl) * kPbStride)[r] = hi;
@@ -513,18 +533,32 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     if (s == 0 && lse != nullptr && cluster_rank() == 0) lse[hg * HG + h] = L > 0.f ? M + logf(L) : -INFINITY;
   }
   __syncthreads();
-#pragma unroll
-  for (int j = 0; j < kQLoads; ++j) {
-    const int e = int(cluster_rank()) * kQLoads * kThreads + j * kThreads + tid;
+  {
+    // HG / 4 consecutive outputs of one head per thread: one vector load per peer
+    constexpr int kV = kQLoads;
+    const int e = (int(cluster_rank()) * kThreads + tid) * kV;
     const int h = e / DS4X_KV_DIM, d = e % DS4X_KV_DIM;
-    float os[kCluster];
+    float os[kCluster][kV];
 #pragma unroll
-    for (int s = 0; s < kCluster; ++s) os[s] = ld_peer(&Opart[h * DS4X_KV_DIM + d], uint32_t(s));
-    float o = 0.f;
-#pragma unroll
-    for (int s = 0; s < kCluster; ++s) o = fmaf(fw[h][s], os[s], o);
+    for (int s = 0; s < kCluster; ++s) ld_peer_vec<kV>(&Opart[h * DS4X_KV_DIM + d], uint32_t(s), os[s]);
     const float L = fl[h];
-    out[size_t(hg * HG + h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+    uint16_t ob[kV];
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      float o = 0.f;
+#pragma unroll
+      for (int s = 0; s < kCluster; ++s) o = fmaf(fw[h][s], os[s][v], o);
+      ob[v] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+    }
+    uint16_t *dst = out + size_t(hg * HG + h) * DS4X_KV_DIM + d;
+    if (kV == 4) {
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(uint32_t(ob[0]) | (uint32_t(ob[kV > 1 ? 1 : 0]) << 16),
+                                                   uint32_t(ob[kV > 2 ? 2 : 0]) | (uint32_t(ob[kV > 3 ? 3 : 0]) << 16));
+    } else if (kV == 2) {
+      *reinterpret_cast<uint32_t *>(dst) = uint32_t(ob[0]) | (uint32_t(ob[kV > 1 ? 1 : 0]) << 16);
+    } else {
+      dst[0] = ob[0];
+    }
   }
   cluster_wait_peers();  // peers may still be reading this CTA's partials
 }
