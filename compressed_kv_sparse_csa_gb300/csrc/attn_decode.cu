@@ -59,6 +59,10 @@ constexpr int kPbStride = 2 * kRows + 16;           // 144 bytes per weight row
 constexpr size_t kKhBytes = size_t(kRows) * kSlotBytes;                     // 66,560
 constexpr size_t kPbBytes = size_t(2) * kBlocks * 8 * kPbStride;            // 18,432: hi and lo parts
 
+// Partial-output rows, in floats: 512 + 4, so the MMA fragments' stores (4
+// heads x 8 columns per warp) hit 32 banks and every row stays 16-byte aligned.
+constexpr int kOpStride = DS4X_KV_DIM + 4;
+
 // Per head-group size: HG = 4 keeps the partial output (8 KB) and the logit
 // halves (2 KB) in their own space; HG >= 8 puts the partial output (16 or
 // 32 KB) over the row slots once the output MMAs are done and the logit
@@ -71,7 +75,7 @@ struct Cfg {
   static constexpr int kNT = HG > 8 ? HG / 8 : 1;  // 8-head n tiles of the logits, passes of the output
   static constexpr int kPH = HG > 8 ? 8 : HG;      // heads per output pass
   static constexpr size_t kQhBytes = size_t(8 * kNT) * kQhStride;  // query rows: the heads, then zero rows
-  static constexpr size_t kOpBytes = size_t(HG) * DS4X_KV_DIM * sizeof(float);
+  static constexpr size_t kOpBytes = size_t(HG) * kOpStride * sizeof(float);
   static constexpr size_t kRedBytes = size_t(2) * kRows * HG * sizeof(float);
   static constexpr size_t kSmemBytes =
       kShared ? kKhBytes + kQhBytes + kPbBytes : kKhBytes + kQhBytes + kPbBytes + kOpBytes + kRedBytes;
@@ -193,9 +197,9 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
   unsigned char *Qh = smem + kKhBytes;                        // [8][1040]: scaled query, fp16
   unsigned char *Pb = Qh + C::kQhBytes;                       // [hi, lo][8 blocks][8][144]: weights, fp16
-  float *Opart = C::kShared ? reinterpret_cast<float *>(Kh)                 // [HG][512]
+  float *Opart = C::kShared ? reinterpret_cast<float *>(Kh)                 // [HG][516]
                             : reinterpret_cast<float *>(Pb + kPbBytes);
-  float *red = C::kShared ? reinterpret_cast<float *>(Pb) : Opart + HG * DS4X_KV_DIM;  // [2][64][HG]
+  float *red = C::kShared ? reinterpret_cast<float *>(Pb) : Opart + HG * kOpStride;  // [2][64][HG]
   // odd row strides: a warp reading one column over 32 rows hits 32 banks
   __shared__ float Pt[kRows][HG + 1];              // logits, then exp(l - m)
   __shared__ float sc[kRows][kBlocks + 1];         // block scales (1 for the RoPE tail)
@@ -459,15 +463,28 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 #pragma unroll
   for (int pass = 0; pass < C::kNT; ++pass) {
     if (pass > 0) __syncthreads();  // the previous pass's MMAs have read the weights
-    for (int e = tid; e < kBlocks * C::kPH * kRows; e += kThreads) {
-      const int blk = e / (C::kPH * kRows), hl = (e / kRows) % C::kPH, r = e % kRows;
-      const int h = C::kPH * pass + hl;
-      const float smax = sbmax[blk];
-      const float w = smax > 0.f ? Pt[r][h] * (sc[r][blk] * sbinv[blk]) : 0.f;  // the ratio is exact
-      const __half hi = __float2half_rn(w);
-      const __half lo = __float2half_rn(w - __half2float(hi));
-      reinterpret_cast<__half *>(Pb + (blk * 8 + hl) * kPbStride)[r] = hi;
-      reinterpret_cast<__half *>(Pb + ((kBlocks + blk) * 8 + hl) * kPbStride)[r] = lo;
+    {
+      // thread t: row t % 64, blocks 2 (t / 64) and + 1; the row's scale
+      // ratios once, each head's exp(l - m) once
+      static_assert(2 * (kThreads / kRows) == kBlocks, "two blocks per thread");
+      const int r = tid % kRows, b0 = 2 * (tid / kRows);
+      float ratio[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        ratio[j] = sbmax[b0 + j] > 0.f ? sc[r][b0 + j] * sbinv[b0 + j] : 0.f;  // exact: powers of two
+#pragma unroll
+      for (int hl = 0; hl < C::kPH; ++hl) {
+        const float pe = Pt[r][C::kPH * pass + hl];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int blk = b0 + j;
+          const float w = pe * ratio[j];
+          const __half hi = __float2half_rn(w);
+          const __half lo = __float2half_rn(w - __half2float(hi));
+          reinterpret_cast<__half *>(Pb + (blk * 8 + hl) * kPbStride)[r] = hi;
+          reinterpret_cast<__half *>(Pb + ((kBlocks + blk) * 8 + hl) * kPbStride)[r] = lo;
+        }
+      }
     }
     __syncthreads();
     const int blk = warp;
@@ -503,10 +520,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int d0 = DS4X_KV_BLOCK * blk + 16 * t + g;
-          Opart[h * DS4X_KV_DIM + d0] = acc[pass][t][0] * smax;
-          Opart[(h + 1) * DS4X_KV_DIM + d0] = acc[pass][t][1] * smax;
-          Opart[h * DS4X_KV_DIM + d0 + 8] = acc[pass][t][2] * smax;
-          Opart[(h + 1) * DS4X_KV_DIM + d0 + 8] = acc[pass][t][3] * smax;
+          Opart[h * kOpStride + d0] = acc[pass][t][0] * smax;
+          Opart[(h + 1) * kOpStride + d0] = acc[pass][t][1] * smax;
+          Opart[h * kOpStride + d0 + 8] = acc[pass][t][2] * smax;
+          Opart[(h + 1) * kOpStride + d0 + 8] = acc[pass][t][3] * smax;
         }
       }
     }
@@ -540,7 +557,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     const int h = e / DS4X_KV_DIM, d = e % DS4X_KV_DIM;
     float os[kCluster][kV];
 #pragma unroll
-    for (int s = 0; s < kCluster; ++s) ld_peer_vec<kV>(&Opart[h * DS4X_KV_DIM + d], uint32_t(s), os[s]);
+    for (int s = 0; s < kCluster; ++s) ld_peer_vec<kV>(&Opart[h * kOpStride + d], uint32_t(s), os[s]);
     const float L = fl[h];
     uint16_t ob[kV];
 #pragma unroll
