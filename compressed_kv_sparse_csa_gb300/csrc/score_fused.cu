@@ -32,10 +32,11 @@
 //    16th key's bucket: the CTA's candidates, published unsorted with a
 //    bound that every key it left out is below;
 //  * the CTAs of a session meet at a bounded barrier (the launch is
-//    cooperative, so all are resident); each then loads all the session's
-//    candidates, finds the k-th largest by a radix select, and writes its
-//    own winners at their ranks (counted against all candidates), so the
-//    merge runs in every CTA at once instead of in the last one.  A CTA
+//    cooperative, so all are resident); each then loads the session's
+//    candidates at or above the largest bound and writes its own winners at
+//    their ranks among them (direct counts for a few candidates, a counting
+//    sort over 2048 buckets for more), so the merge runs in every CTA at
+//    once instead of in the last one.  A CTA
 //    whose bound beats the k-th key may hold more winners: then every such
 //    CTA publishes its superset and the session's first CTA merges exactly.
 //
@@ -77,9 +78,9 @@ constexpr int kCandCap = kLocalK + 64;     // candidates a CTA may publish (its 
 constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged CTA may publish
 constexpr int kPoolPer = 8;                // pool keys each selection thread holds in registers
 constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
-constexpr int kRadixBuckets = 2048;        // radix-select histogram over the pool
+constexpr int kRadixBuckets = 2048;        // counting-sort buckets over the kept pool keys
 constexpr int kRankStep = 8;              // candidates ranked together (lane j stores candidate j's partial)
-constexpr int kDirect = 256;               // up to this many candidates a CTA ranks by direct counts
+constexpr int kDirect = 16;                // up to this many candidates a CTA ranks by direct counts
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
@@ -138,7 +139,6 @@ struct __align__(1024) Smem {
   unsigned long long keys[kKeysCap];          // [0, 512): carried keys; then the chunk's keys
   unsigned long long out[kLocalK];
   unsigned long long sortbuf[2 * kLocalK];
-  unsigned long long small[32];               // the radix select's last bucket
   alignas(16) uint32_t hist[kHistWords];      // fixed histogram, or the adaptive one inside select_top
   alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
   uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
@@ -454,35 +454,27 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
   return sh.out_cnt;
 }
 
-// The need-th largest of the distinct nonzero keys of pool[0, n) that lie
-// in [lo, hi] (1 <= need <= their count), by
-// radix select: each pass histograms those keys into 2048 buckets spanning
-// [lo, hi] (bucket 0: the top), finds the bucket where the count from the top
-// reaches `need` and narrows [lo, hi] to it; a bucket of at most 32 keys is
-// finished by ranking its keys against each other.  hist[0, 2048) must be
-// zero on entry (and is again on return); sh.ncol must be zero; small holds
-// 32 keys.  Returns the same value in every thread.
-__device__ unsigned long long kth_regs(const unsigned long long *pool, int n, unsigned long long lo,
-                                       unsigned long long hi, int need, uint32_t *hist,
-                                       unsigned long long *small, SelShared &sh, int tid) {
+// Ranks of cand[0, nc) (this CTA's keys, all among pool[0, n)) among the n
+// distinct nonzero keys of pool[0, n), all in [lo, hi]: a counting sort over
+// 2048 buckets spanning [lo, hi] (bucket 0: the top), so a key's rank is the
+// number of keys in higher buckets plus those of its own bucket above it.
+// A candidate of rank r < k goes to out_idx[r] (and out_score[r]).
+// hist[0, 2048) must be zero on entry; sorted holds n keys.
+__device__ void bucket_rank(const unsigned long long *pool, int n, const unsigned long long *cand, int nc,
+                            unsigned long long lo, unsigned long long hi, int k, uint32_t *hist,
+                            unsigned long long *sorted, SelShared &sh, int tid, int32_t *out_idx,
+                            float *out_score) {
   constexpr int kB = kRadixBuckets;
   static_assert(kB == 4 * kWGThreads, "four buckets per thread");
   const int lane = tid & 31, warp = tid >> 5;
-  for (int pass = 0; pass < 8; ++pass) {
-    const unsigned long long range = hi - lo;
-    const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 11;  // range >> shift < 2048
-#pragma unroll
-    for (int q = 0; q < kPoolPer; ++q) {
-      const int i = q * kWGThreads + tid;
-      const unsigned long long x = i < n ? pool[i] : 0ull;
-      if (x != 0ull && x >= lo && x <= hi) atomicAdd(&hist[kB - 1 - int((x - lo) >> shift)], 1u);
-    }
-    bar512();
-    // thread t owns buckets [4t, 4t + 4); it alone reads them, then clears them
+  const unsigned long long range = hi - lo;
+  const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 11;  // range >> shift < 2048
+  auto bucket = [&](unsigned long long x) { return kB - 1 - int((x - lo) >> shift); };
+  for (int i = tid; i < n; i += kWGThreads) atomicAdd(&hist[bucket(pool[i])], 1u);
+  bar512();
+  {  // exclusive scan in place: hist[b] = keys in the buckets above b (thread t: buckets 4t .. 4t + 3)
     const uint4 c4 = reinterpret_cast<const uint4 *>(hist)[tid];
-    reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
-    const int local = int(c[0] + c[1] + c[2] + c[3]);
+    const int local = int(c4.x + c4.y + c4.z + c4.w);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -494,52 +486,31 @@ __device__ unsigned long long kth_regs(const unsigned long long *pool, int n, un
     int above = incl - local;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int4 s = reinterpret_cast<const int4 *>(sh.scan)[j];
-      above += (4 * j < warp ? s.x : 0) + (4 * j + 1 < warp ? s.y : 0) + (4 * j + 2 < warp ? s.z : 0) +
-               (4 * j + 3 < warp ? s.w : 0);
+      const int4 sc4 = reinterpret_cast<const int4 *>(sh.scan)[j];
+      above += (4 * j < warp ? sc4.x : 0) + (4 * j + 1 < warp ? sc4.y : 0) + (4 * j + 2 < warp ? sc4.z : 0) +
+               (4 * j + 3 < warp ? sc4.w : 0);
     }
-    if (above < need && above + local >= need) {
-      int acc = above;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (acc < need && acc + int(c[j]) >= need) {
-          sh.bstar = 4 * tid + j;
-          sh.above = acc;
-          sh.bcnt = int(c[j]);
-        }
-        acc += int(c[j]);
-      }
-    }
-    bar512();
-    const int bs = sh.bstar, bc = sh.bcnt;
-    need -= sh.above;
-    const unsigned long long blo = lo + (static_cast<unsigned long long>(kB - 1 - bs) << shift);
-    const unsigned long long width_m1 = shift == 0 ? 0ull : ((1ull << shift) - 1ull);
-    const unsigned long long bhi = (hi - blo > width_m1) ? blo + width_m1 : hi;
-    if (bc <= 32) {
-#pragma unroll
-      for (int q = 0; q < kPoolPer; ++q) {
-        const int i = q * kWGThreads + tid;
-        const unsigned long long x = i < n ? pool[i] : 0ull;
-        if (x != 0ull && x >= blo && x <= bhi) {
-          const int slot = atomicAdd(&sh.ncol, 1);
-          if (slot < 32) small[slot] = x;
-        }
-      }
-      bar512();
-      if (warp == 0) {
-        const unsigned long long x = lane < bc ? small[lane] : 0ull;
-        int r = 0;
-        for (int j = 0; j < bc; ++j) r += small[j] > x;
-        if (lane < bc && r == need - 1) sh.cut = x;
-      }
-      bar512();
-      return sh.cut;
-    }
-    lo = blo;
-    hi = bhi;
+    const uint32_t a0 = uint32_t(above), a1 = a0 + c4.x, a2 = a1 + c4.y, a3 = a2 + c4.z;
+    reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(a0, a1, a2, a3);
   }
-  return lo;  // not reached for distinct 64-bit keys (each pass keeps <= 2^-11 of the range)
+  bar512();
+  for (int i = tid; i < n; i += kWGThreads) {  // counting-sort scatter: bucket by bucket, from the top
+    const unsigned long long x = pool[i];
+    sorted[atomicAdd(&hist[bucket(x)], 1u)] = x;
+  }
+  bar512();
+  // hist[b] is now the end of bucket b, the start of bucket b + 1
+  for (int e = tid; e < nc; e += kWGThreads) {
+    const unsigned long long x = cand[e];
+    const int b = bucket(x);
+    const int s0 = b == 0 ? 0 : int(hist[b - 1]), s1 = int(hist[b]);
+    int r = s0;
+    for (int j = s0; j < s1; ++j) r += sorted[j] > x ? 1 : 0;
+    if (r < k) {
+      out_idx[r] = key_index(x);
+      if (out_score) out_score[r] = key_score(x);
+    }
+  }
 }
 
 // Grid-scope release add and acquire load (the arrival and the poll of the
@@ -1056,7 +1027,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
         for (int i = tid; i < ncand; i += kWGThreads) pool_g[base + i] = sm.cand[i];
         if (tid == 0) atomicMax(&ss.thm[par], th);
       }
-      reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the radix select's 2048 buckets
+      reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the counting sort's 2048 buckets
       if (tid == 0) {
         sm.sel.ncol = 0;
         sm.sel.nhi = 0;
@@ -1189,54 +1160,17 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
               }
             }
           } else {
-            unsigned long long cut = 1ull;  // n_all <= k: every candidate wins
-            if (n_all > k) {
-              uint32_t mn = ~0u, mx = 0u;
-              for (int w = 0; w < kWGThreads / 32; ++w) {
-                mn = min(mn, sm.sel.red_lo[w]);
-                mx = max(mx, sm.sel.red_hi[w]);
-              }
-              const unsigned long long lo = static_cast<unsigned long long>(mn) << 32;
-              const unsigned long long hi = (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull;
-              cut = kth_regs(pool_s, n_ge, lo, hi, k, sm.hist, sm.small, sm.sel, tid);
+            // more candidates: a counting sort of the kept pool keys ranks them all at once
+            uint32_t mn = ~0u, mx = 0u;
+            for (int w = 0; w < kWGThreads / 32; ++w) {
+              mn = min(mn, sm.sel.red_lo[w]);
+              mx = max(mx, sm.sel.red_hi[w]);
             }
-            {  // the winners, every pool key at or above the cut, into out[] (ballots taken twice)
-              int cnt = 0;
-#pragma unroll
-              for (int q = 0; q < kPoolPer; ++q) {
-                const int i = q * kWGThreads + tid;
-                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
-                cnt += __popc(__ballot_sync(0xffffffffu, pv != 0ull && pv >= cut));
-              }
-              int base = 0;
-              if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.wcnt, cnt);
-              base = __shfl_sync(0xffffffffu, base, 0);
-              const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-              for (int q = 0; q < kPoolPer; ++q) {
-                const int i = q * kWGThreads + tid;
-                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
-                const bool win = pv != 0ull && pv >= cut;
-                const unsigned mk = __ballot_sync(0xffffffffu, win);
-                const int p = base + __popc(mk & lt);
-                if (win && p < kLocalK) sm.out[p] = pv;
-                base += __popc(mk);
-              }
-            }
-            bar512();
-            const int nw = min(sm.sel.wcnt, kLocalK);
-            // this CTA's winners, each at its rank among all winners
-            for (int e = warp; e < ncand; e += kWGThreads / 32) {
-              const unsigned long long x = sm.cand[e];
-              if (x < cut) continue;
-              int r = 0;
-              for (int i = lane; i < nw; i += 32) r += sm.out[i] > x ? 1 : 0;
-              r = __reduce_add_sync(0xffffffffu, r);
-              if (lane == 0 && r < k) {
-                out_idx[r] = key_index(x);
-                if (out_score) out_score[r] = key_score(x);
-              }
-            }
+            const unsigned long long lo = static_cast<unsigned long long>(mn) << 32;
+            const unsigned long long hi = (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull;
+            static_assert(2 * kPoolCap * 8 <= kStages * kTileBytes, "the pool and its sorted copy fit the stage ring");
+            bucket_rank(pool_s, n_ge, sm.sortbuf, nhi, lo, hi, k, sm.hist, pool_s + kPoolCap, sm.sel, tid, out_idx,
+                        out_score);
           }
           if (int(blockIdx.x) == cta0) {
             for (int e = nwin + tid; e < k; e += kWGThreads) {
