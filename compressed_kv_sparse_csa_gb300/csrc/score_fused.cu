@@ -703,6 +703,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  bool lo_nonzero = false;
   if (tid < kWGThreads) {
     // query -> two E4M3 pieces per 32-element block (B rows h and 64 + h);
     // thread t < 256 takes head t / 4, block t % 4 (32 elements, 64 bytes)
@@ -754,6 +755,8 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           make_uint4(lw[4], lw[5], lw[6], lw[7]);
       sm.sfb[h][b] = uint8_t(e_hi + 127);
       sm.sfb[DS4X_IDX_HEADS + h][b] = uint8_t(e_lo + 127);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) lo_nonzero |= (lw[j] & 0x7f7f7f7fu) != 0u;  // any nonzero lo code (0x80 is -0)
     }
     for (int h = tid; h < DS4X_IDX_HEADS; h += kWGThreads) sm.wq[h] = w[h];
     for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
@@ -761,7 +764,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   }
   fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
+  // the barrier also tells every thread whether the query has a lo piece: a
+  // query that is exact in E4M3 (prefill) needs only the hi MMAs
+  const bool lo_any = __syncthreads_or(lo_nonzero ? 1 : 0) != 0;
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
   if (warp < 4) {
@@ -809,9 +814,13 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
         if (!wait_bar(sm, &sm.afull[a], (i / kASlots) & 1, hdr)) break;
         if (i >= kDSlots && !wait_seq(sm, &sm.dfree[d], i - kDSlots, hdr)) break;
         tc_fence_after();
-        mma_mxf8f6f4_ta_k128_2b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a), bdesc_hi,
-                                bdesc_lo, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a), tmem_base + kSfbCol,
-                                tmem_base + kSfbLoCol);
+        if (lo_any)
+          mma_mxf8f6f4_ta_k128_2b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a),
+                                  bdesc_hi, bdesc_lo, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a),
+                                  tmem_base + kSfbCol, tmem_base + kSfbLoCol);
+        else
+          mma_mxf8f6f4_ta_k128_1b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a),
+                                  bdesc_hi, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a), tmem_base + kSfbCol);
         tc_commit(smem_u32(&sm.aempty[a]));
         tc_commit(smem_u32(&sm.dfull[d]));
         issued = i + 1;

@@ -152,6 +152,24 @@ __device__ __forceinline__ void mma_mxf8f6f4_ta_k128_2b(uint32_t d_tmem, uint32_
       : "memory");
 }
 
+// The same with one B operand (the query's lo piece is all zero): four MMAs,
+// K step s reading scale-factor byte s.
+__device__ __forceinline__ void mma_mxf8f6f4_ta_k128_1b(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc0,
+                                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 a, id;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], pf;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 16;\n\tor.b32 id, %3, 0x20000010;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b, id, [%4], [%5], pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\tor.b32 id, %3, 0x40000020;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b, id, [%4], [%5], pt;\n\t"
+      "add.u32 a, a, 8;\n\tadd.s64 b, b, 16;\n\tor.b32 id, %3, 0x60000030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [a], b, id, [%4], [%5], pt;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc0), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // tcgen05.st of one / four 32-bit columns (32 lanes x 32 bits each).
 __device__ __forceinline__ void tc_st_x1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
