@@ -624,6 +624,7 @@ def run_prefill(args):
     per-query sparse attention."""
     torch, B, dev, stream = _gpu_setup()
     T, n, base = 2048, 65536, 63488
+    per_launch = min(torch.cuda.get_device_properties(dev).multi_processor_count, 256)  # sessions per scorer launch
     gen = torch.Generator(device=dev)
     gen.manual_seed(4004)
     with torch.cuda.stream(stream):
@@ -696,8 +697,8 @@ def run_prefill(args):
                      "peak_kind": "measured bf16 burst x 2 (FP8 nominal ratio)", "traffic": None,
                      "attention_tflops": flop_attn / (parts["attend"] * 1e-3) / 1e12},
         # per step: the quantiser, the prefill set-up kernel, one scorer launch per
-        # DS4X_MAX_SESSIONS (64) query tokens, and one attention launch
-        "gpu_launches": steps * (3 + (T + 63) // 64), "clocks": clk.summary()}), flush=True)
+        # SM-count query tokens (one session per CTA), and one attention launch
+        "gpu_launches": steps * (3 + (T + per_launch - 1) // per_launch), "clocks": clk.summary()}), flush=True)
 
 if __name__ == "__main__":
     main()

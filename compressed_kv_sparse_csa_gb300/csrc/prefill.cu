@@ -12,7 +12,9 @@
 //   and writes, per query token i, the session it is scored as: the same
 //   indexer rows with the causal length min(n_rows, causal_base + i).
 // * The scoring itself is the fused block-scaled scorer run as a batch of
-//   such sessions (launch_score_batch), up to DS4X_MAX_SESSIONS per launch;
+//   such sessions (launch_score_batch), as many per launch as it has CTAs
+//   (one per SM), spread evenly over the launches: every CTA then streams
+//   one whole session, so no launch waits on a session with fewer CTAs;
 //   its query split gives hi = the exact E4M3 value and lo = 0 for such a
 //   query, so every product is exact and the sums are fp32.
 #include <cuda_bf16.h>
@@ -112,8 +114,13 @@ cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const 
                                                                          causal_base, qbf, rows_arr, n_arr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  for (int32_t c0 = 0; c0 < T; c0 += DS4X_MAX_SESSIONS) {
-    const int32_t ns = T - c0 < DS4X_MAX_SESSIONS ? T - c0 : DS4X_MAX_SESSIONS;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int32_t cap = sms < score_fused_max_ctas() ? sms : score_fused_max_ctas();  // sessions per launch
+  const int32_t launches = (T + cap - 1) / cap;
+  for (int32_t c0 = 0, li = 0; c0 < T; ++li) {
+    const int32_t ns = (T - c0 + (launches - li) - 1) / (launches - li);  // the rest, spread evenly
     ScoreBatch sb{};
     sb.rows_arr = rows_arr + c0;
     sb.n_arr = n_arr + c0;
@@ -125,6 +132,7 @@ cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const 
     sb.out_score = out_score != nullptr ? out_score + size_t(c0) * k : nullptr;
     e = launch_score_batch(sb, 0, base + L.fused, stream);
     if (e != cudaSuccess) return e;
+    c0 += ns;
   }
   return cudaSuccess;
 }

@@ -84,8 +84,10 @@ constexpr int kDirect = 16;                // up to this many candidates a CTA r
 constexpr int kBuckets = 8192;             // fixed score-bit histogram (16-bit counters, 2 per word)
 constexpr int kHistWords = 4096;
 constexpr int kMaxCtas = 256;
-constexpr int kMaxSess = DS4X_MAX_SESSIONS;   // sessions one batched call may score
+constexpr int kMaxSess = 256;              // sessions one launch may score (the batched API allows
+                                           // DS4X_MAX_SESSIONS; the prefill path one per CTA)
 constexpr int kTmemCols = 512;
+static_assert(kMaxSess >= kMaxCtas && kMaxSess >= DS4X_MAX_SESSIONS, "one session per CTA fits");
 constexpr int kN = DS4X_IDX_HEADS;         // 64 heads per MMA; B rows 0-63 hold the hi pieces, 64-127 the lo pieces
 constexpr uint32_t kDCol0 = 0;             // D slot j: columns [64 j, 64 j + 64)
 constexpr uint32_t kACol0 = 64 * kDSlots;  // A slot a: 32 columns from kACol0 + 32 a

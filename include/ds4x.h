@@ -269,7 +269,7 @@ int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, u
  *
  * and gets the exact top-k of its visible rows (score descending, lower
  * index first; -1 / NaN past its visible count).  Run as the fused scorer
- * over one "session" per query token (up to DS4X_MAX_SESSIONS per launch).
+ * over one "session" per query token (one per SM per launch).
  *
  *   idx_rows   u8 [n_rows][68]
  *   q_codes    u8 [n_queries][64][128], q_scales u8 [n_queries][64][4]
