@@ -71,8 +71,12 @@ constexpr int kASlots = 6;                 // tensor-memory A ring
 constexpr int kDSlots = 4;                 // tensor-memory accumulator ring
 constexpr int kChunkTiles = 64;
 constexpr int kLocalK = DS4X_TOPK_MAX;     // 512
-constexpr int kKeysCap = kLocalK + kChunkTiles * kTileRows;  // 8704
-constexpr int kSelPerThread = 17;          // 17 * 512 >= kKeysCap and >= 256 * 16 + 512
+// Keys carried from one chunk to the next: every key at or above the bucket
+// of the CTA's 512th, at most 1024 of them (an exact selection cuts them to
+// 512 only beyond that).
+constexpr int kCarry = 2 * kLocalK;         // 1024
+constexpr int kKeysCap = kCarry + kChunkTiles * kTileRows;  // 9216
+constexpr int kSelPerThread = 18;          // 18 * 512 >= kKeysCap
 constexpr int kTopM = 16;                  // fewest candidates a CTA publishes
 constexpr int kCandCap = kLocalK + 64;     // candidates a CTA may publish (its top M and their bucket)
 constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged CTA may publish
@@ -115,6 +119,7 @@ static_assert(kDSlots * 64 <= int(kACol0) && kACol0 + 32 * kASlots <= kSfaCol0 &
 static_assert(kSfaCol0 % 4 == 0 && kSfbCol % 4 == 0 && kSfbLoCol % 4 == 0,
               "scale-factor columns start on a 4-column boundary");
 static_assert(kSelPerThread * kWGThreads >= kKeysCap, "selection registers cover the key buffer");
+static_assert(kKeysCap * 8 <= kStages * kTileBytes, "the key buffer fits the stage ring (the exact top-M copy)");
 constexpr int kMaxDynSmem = 232448;         // 227 KB per CTA on sm_103
 
 // Byte offset of (row r, K element kk) in a canonical no-swizzle K-major
@@ -138,7 +143,7 @@ struct SelShared {
 struct __align__(1024) Smem {
   uint8_t bq[kOpBytes];                       // query pieces, E4M3, canonical K-major (B)
   uint8_t stage[kStages][kTileBytes];         // raw tile ring
-  unsigned long long keys[kKeysCap];          // [0, 512): carried keys; then the chunk's keys
+  unsigned long long keys[kKeysCap];          // [0, 1024): carried keys; then the chunk's keys
   unsigned long long out[kLocalK];
   unsigned long long sortbuf[2 * kLocalK];
   alignas(16) uint32_t hist[kHistWords];      // fixed histogram, or the adaptive one inside select_top
@@ -905,13 +910,13 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
             key = make_key(s_row, uint32_t(row));
             hist_add(sm.hist, fixed_bucket(key));
           }
-          sm.keys[kLocalK + (i - c0) * kTileRows + r] = key;
+          sm.keys[kCarry + (i - c0) * kTileRows + r] = key;
         }
       }
       bar512();
 
       // ---- end of chunk ---------------------------------------------------------
-      const int n_in = kLocalK + (c1 - c0) * kTileRows;
+      const int n_in = kCarry + (c1 - c0) * kTileRows;
       if (c1 == n_tiles) {  // the last chunk's keys stay in place for the exchange below
         last_n_in = n_in;
         break;
@@ -949,11 +954,12 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       }
       bar512();
       int n_keep = sm.sel.list_cnt;
-      for (int i = n_keep + tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
+      // the rest of the carried region is zero (the chunk region is rewritten whole)
+      for (int i = n_keep + tid; i < kCarry; i += kWGThreads) sm.keys[i] = 0ull;
       bar512();
-      if (n_keep > kLocalK) {  // a wide boundary bucket: reduce exactly to 512
+      if (n_keep > kCarry) {  // a very wide boundary bucket: reduce exactly to 512
         const int m = select_top(sm.keys, n_keep, kLocalK, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-        for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = i < m ? sm.out[i] : 0ull;
+        for (int i = tid; i < kCarry; i += kWGThreads) sm.keys[i] = i < m ? sm.out[i] : 0ull;
         bar512();
         n_keep = m;
       }
