@@ -27,7 +27,7 @@
 //   4. the cluster combines its 8 partials through distributed shared
 //      memory, o_h = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s: each CTA
 //      finishes 1/8 of the group's HG x 512 outputs, and the LSE M + log L.
-// About 95 KB (HG = 4), 98 KB (HG = 8) or 107 KB (HG = 16) of shared memory
+// About 106 KB (HG = 4), 99 KB (HG = 8) or 107 KB (HG = 16) of shared memory
 // per CTA, so two CTAs fit an SM: from HG = 8 on, the partial output reuses
 // the row slots and the logit halves the weight buffer, and HG = 16 makes
 // its weights and output MMAs in two passes of 8 heads.  The n = 8 side of
