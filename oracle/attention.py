@@ -47,3 +47,43 @@ def sparse_attn_decode(kv_rows, idx, q_bf16, scale: float):
     out = (e / denom) @ v
     lse = mx[:, 0] + np.log(denom[:, 0])
     return bf16_round(out), out, lse
+
+
+def dense_attn_decode(kv_rows, n: int, q_bf16, scale: float):
+    """Dense decode attention over every row [0, n) -- the HCA layers' exact
+    attention over all their compressed rows (DS4X README, "Optimization
+    details", the HCA bullet: exact score-split attention with no row
+    ceiling).  Same definition as the sparse attention with every row
+    selected; written out on its own.  Returns (out bf16-rounded, out_exact,
+    lse), float64, shapes [H, 512], [H, 512], [H]; n = 0 gives zeros and -inf.
+    """
+    q = bf16_decode(q_bf16)
+    heads, dim = q.shape
+    if n <= 0:
+        zero = np.zeros((heads, dim))
+        return zero, zero, np.full(heads, -np.inf)
+    v = unpack_kv_rows(np.asarray(kv_rows)[:n])  # [n, 512]
+    logits = float(scale) * (q @ v.T)  # [H, n]
+    m = logits.max(axis=1)
+    w = np.exp(logits - m[:, None])
+    s = w.sum(axis=1)
+    out = (w @ v) / s[:, None]
+    return bf16_round(out), out, m + np.log(s)
+
+
+def lse_combine(parts):
+    """The split-KV log-sum-exp combine (the benchmark spec's split-KV
+    flash-decoding; DS4X README, "Nsight Systems", the score-split finalize):
+    parts is a list of (o_s [H, D] normalised within split s, lse_s [H]); an
+    empty split has lse -inf.  Returns (o, lse) with
+        M = max_s lse_s,  o = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M),
+        lse = M + log sum_s e^(lse_s - M).
+    """
+    lse = np.stack([np.asarray(p[1], dtype=np.float64) for p in parts])  # [S, H]
+    o = np.stack([np.asarray(p[0], dtype=np.float64) for p in parts])  # [S, H, D]
+    m = lse.max(axis=0)  # [H]
+    safe_m = np.where(np.isfinite(m), m, 0.0)
+    f = np.where(np.isfinite(lse), np.exp(lse - safe_m[None, :]), 0.0)  # [S, H]
+    tot = f.sum(axis=0)
+    out = np.where(tot[:, None] > 0, (f[:, :, None] * o).sum(axis=0) / np.where(tot > 0, tot, 1.0)[:, None], 0.0)
+    return out, np.where(tot > 0, safe_m + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
