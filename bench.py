@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode attn step latency (µs/layer) & compressed rows/s vs N; achieved HBM GB/s"
 WORKLOADS = {"tiny": 4096, "mid": 131072, "long": 1048576}
-EXTRA_WORKLOADS = ("sessions", "prefill")  # parity configurations, measured on request
+EXTRA_WORKLOADS = ("sessions", "prefill", "hca")  # parity configurations, measured on request
 K_TOP = 512
 HEADS = 64
 FALLBACK_HBM_GBS = 6800.0
@@ -261,7 +261,7 @@ def main():
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode workloads only"}))
             return
-        (run_sessions if args.workload == "sessions" else run_prefill)(args)
+        {"sessions": run_sessions, "prefill": run_prefill, "hca": run_hca}[args.workload](args)
         return
     n = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -615,6 +615,59 @@ def run_sessions(args):
                      "achieved": sb / (ms_sc * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": sb / (ms_sc * 1e-3) / 1e9 / peak, "traffic": None, "us_per_launch": ms_sc * 1e3,
                      "peak_kind": kind},
+        "gpu_launches": steps * 2, "clocks": clk.summary()}), flush=True)
+
+
+def run_hca(args):
+    """Dense decode attention over every compressed row of a ratio-128 (HCA)
+    layer at a 1M-token context: 8192 rows of 583 B, 64 heads; 40 layer
+    copies (191 MB, above the 129 MB L2) rotated, one CUDA graph per layer
+    (the 512-row tiles' attention and the finalize)."""
+    torch, B, dev, stream = _gpu_setup()
+    n, L = 8192, 40
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6006)
+    layers = []
+    with torch.cuda.stream(stream):
+        for _ in range(L):
+            kv = torch.empty(n * 583, dtype=torch.uint8, device=dev)
+            B.ds4x_cache_append(kv, None, 0, torch.randn((n, 512), generator=gen, device=dev), None, stream=stream)
+            layers.append({"kv": kv, "q": torch.randn((64, 512), generator=gen, device=dev).to(torch.bfloat16),
+                           "out": torch.empty((64, 512), dtype=torch.bfloat16, device=dev)})
+        ws = torch.empty(B.ds4x_dense_attn_decode_workspace(n), dtype=torch.uint8, device=dev)
+        B.ds4x_workspace_init(ws, stream=stream)
+    stream.synchronize()
+    scale = 1.0 / math.sqrt(512.0)
+
+    def step(c):
+        B.ds4x_dense_attn_decode(c["kv"], n, c["q"], scale, c["out"], None, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(layers[i % L])
+    stream.synchronize()
+    graphs = []
+    for c in layers:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    steps = min(args.steps, 2000)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        ms = _timed_graph(torch, stream, graphs, steps, args.warmup)
+    peak, kind = measured_peak()
+    algo = n * 583 + 2 * 64 * 512 * 2  # the rows, the query, the output
+    print(json.dumps({
+        "metric": "HCA dense decode attention latency (us) & compressed rows/s",
+        "value": n / (ms * 1e-3), "unit": "compressed rows/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-in/fp32-acc (E4M3/FP16 packed rows)", "data": "synthetic",
+        "config": {"workload": "dense attention over 8192 ratio-128 rows (1M-token context), 64 heads",
+                   "n_rows": n, "layer_copies": L, "l2": "inputs larger than L2: 40 x 4.8 MB rotated",
+                   "us_per_step": ms * 1e3},
+        "roofline": {"kernel": "ds4x_dense_attn_decode", "bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": algo / (ms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": algo, "peak_kind": kind},
         "gpu_launches": steps * 2, "clocks": clk.summary()}), flush=True)
 
 

@@ -178,7 +178,10 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
   return v;
 }
 
-template <int HG>
+// DENSE: item b is the tile of rows [512 b, 512 b + 512) (no index list),
+// every item reads the one query, and the normalised output goes to out_f32
+// in fp32 for the finalize.
+template <int HG, bool DENSE>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
 attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   using C = Cfg<HG>;
@@ -189,9 +192,9 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   const int64_t n_rows = ab.n_arr != nullptr ? ab.n_arr[bz] : ab.n_rows;
   const int k = ab.k;
   const float scale = ab.scale;
-  const int32_t *__restrict__ idx = ab.idx + size_t(bz) * k;
-  const uint16_t *__restrict__ q = ab.q + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
-  uint16_t *__restrict__ out = ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
+  const int32_t *__restrict__ idx = DENSE ? nullptr : ab.idx + size_t(bz) * k;
+  const uint16_t *__restrict__ q = ab.q + (ab.q_shared ? size_t(0) : size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM);
+  uint16_t *__restrict__ out = DENSE ? nullptr : ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
   float *__restrict__ lse = ab.lse != nullptr ? ab.lse + size_t(bz) * DS4X_ATTN_HEADS : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
@@ -230,7 +233,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   if (tid < kRows) {
     const int j = split * kRows + tid;
     int64_t r = -1;
-    if (j < k) {
+    if (DENSE) {
+      const int64_t t = int64_t(bz) * DS4X_TOPK_MAX + j;  // the tile's rows
+      r = t < n_rows ? t : -1;
+    } else if (j < k) {
       r = idx[j];
       if (r < -1 || r >= n_rows) {
         atomicExch(&hdr->status, int32_t(DS4X_EDEVICE));
@@ -559,22 +565,34 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 #pragma unroll
     for (int s = 0; s < kCluster; ++s) ld_peer_vec<kV>(&Opart[h * kOpStride + d], uint32_t(s), os[s]);
     const float L = fl[h];
+    float of[kV];
     uint16_t ob[kV];
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
       float o = 0.f;
 #pragma unroll
       for (int s = 0; s < kCluster; ++s) o = fmaf(fw[h][s], os[s][v], o);
-      ob[v] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+      of[v] = L > 0.f ? o / L : 0.f;
+      ob[v] = __bfloat16_as_ushort(__float2bfloat16_rn(of[v]));
     }
-    uint16_t *dst = out + size_t(hg * HG + h) * DS4X_KV_DIM + d;
-    if (kV == 4) {
+    if (DENSE) {  // the tile's normalised output in fp32, for the finalize
+      float *fdst = ab.out_f32 + (size_t(bz) * DS4X_ATTN_HEADS + size_t(hg * HG + h)) * DS4X_KV_DIM + d;
+      if (kV == 4) {
+        *reinterpret_cast<float4 *>(fdst) = make_float4(of[0], of[kV > 1 ? 1 : 0], of[kV > 2 ? 2 : 0], of[kV > 3 ? 3 : 0]);
+      } else if (kV == 2) {
+        *reinterpret_cast<float2 *>(fdst) = make_float2(of[0], of[kV > 1 ? 1 : 0]);
+      } else {
+        fdst[0] = of[0];
+      }
+    } else if (kV == 4) {
+      uint16_t *dst = out + size_t(hg * HG + h) * DS4X_KV_DIM + d;
       *reinterpret_cast<uint2 *>(dst) = make_uint2(uint32_t(ob[0]) | (uint32_t(ob[kV > 1 ? 1 : 0]) << 16),
                                                    uint32_t(ob[kV > 2 ? 2 : 0]) | (uint32_t(ob[kV > 3 ? 3 : 0]) << 16));
     } else if (kV == 2) {
+      uint16_t *dst = out + size_t(hg * HG + h) * DS4X_KV_DIM + d;
       *reinterpret_cast<uint32_t *>(dst) = uint32_t(ob[0]) | (uint32_t(ob[kV > 1 ? 1 : 0]) << 16);
     } else {
-      dst[0] = ob[0];
+      out[size_t(hg * HG + h) * DS4X_KV_DIM + d] = ob[0];
     }
   }
   cluster_wait_peers();  // peers may still be reading this CTA's partials
@@ -584,11 +602,11 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 
 size_t attn_decode_ws_bytes(int32_t) { return kWsHeaderBytes; }
 
-template <int HG>
+template <int HG, bool DENSE = false>
 cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
   using C = Cfg<HG>;
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = set_max_smem_once(attn_decode_kernel<HG>, int(C::kSmemBytes), smem_set);
+  cudaError_t e = set_max_smem_once(attn_decode_kernel<HG, DENSE>, int(C::kSmemBytes), smem_set);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the CTAs may start while the previous
   // kernel finishes (it lets them go from its tail); the kernel waits for it
@@ -603,10 +621,11 @@ cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<HG>, ab, static_cast<WsHeader *>(ws));
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<HG, DENSE>, ab, static_cast<WsHeader *>(ws));
 }
 
-cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+template <bool DENSE>
+cudaError_t launch_attn_items(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
   // the fewest heads per cluster whose grid fits one wave (two CTAs per SM):
   // the most CTAs, the shortest latency; beyond that 16, a quarter of the
   // CTAs of 4 heads for about twice the MMAs each (no zero rows)
@@ -615,9 +634,99 @@ cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStre
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t wave = 2 * int64_t(sms);
-  if (int64_t(batch) * kCluster * Cfg<4>::kGroups <= wave) return launch_attn_hg<4>(ab, batch, ws, stream);
-  if (int64_t(batch) * kCluster * Cfg<8>::kGroups <= wave) return launch_attn_hg<8>(ab, batch, ws, stream);
-  return launch_attn_hg<16>(ab, batch, ws, stream);
+  if (int64_t(batch) * kCluster * Cfg<4>::kGroups <= wave) return launch_attn_hg<4, DENSE>(ab, batch, ws, stream);
+  if (int64_t(batch) * kCluster * Cfg<8>::kGroups <= wave) return launch_attn_hg<8, DENSE>(ab, batch, ws, stream);
+  return launch_attn_hg<16, DENSE>(ab, batch, ws, stream);
+}
+
+cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+  return launch_attn_items<false>(ab, batch, ws, stream);
+}
+
+namespace {
+
+// The dense attention's workspace: the status header, then per 512-row tile
+// t the LSEs [t][64] and the normalised outputs [t][64][512], fp32.
+struct DenseWsLayout {
+  size_t lse, o, total;
+};
+DenseWsLayout dense_layout(int64_t n_rows) {
+  const int64_t tiles = (n_rows + DS4X_TOPK_MAX - 1) / DS4X_TOPK_MAX;
+  DenseWsLayout L{};
+  L.lse = kWsHeaderBytes;
+  L.o = L.lse + ((size_t(tiles) * DS4X_ATTN_HEADS * sizeof(float) + 255) / 256) * 256;
+  L.total = L.o + size_t(tiles) * DS4X_ATTN_HEADS * DS4X_KV_DIM * sizeof(float);
+  return L;
+}
+
+// The split-KV combine over the tiles, one head per block: with M the largest
+// tile LSE, o = sum_t e^(lse_t - M) o_t / sum_t e^(lse_t - M) (o_t each tile's
+// normalised output), lse = M + log sum_t e^(lse_t - M).  Tile weights in
+// shared memory (T floats).
+__global__ void __launch_bounds__(256) dense_finalize_kernel(const float *__restrict__ lse_part,
+                                                             const float *__restrict__ o_part, int T,
+                                                             uint16_t *__restrict__ out, float *__restrict__ lse) {
+  extern __shared__ float fsh[];  // [T]: e^(lse_t - M)
+  __shared__ float red[8];
+  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float m = -INFINITY;
+  for (int t = tid; t < T; t += 256) m = fmaxf(m, lse_part[size_t(t) * DS4X_ATTN_HEADS + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();  // red is reused below
+  float sum = 0.f;
+  for (int t = tid; t < T; t += 256) {
+    const float l = lse_part[size_t(t) * DS4X_ATTN_HEADS + h];
+    const float f = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
+    fsh[t] = f;
+    sum += f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[warp] = sum;
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) L += red[w];
+  for (int d = tid; d < DS4X_KV_DIM; d += 256) {
+    float o = 0.f;
+    for (int t = 0; t < T; ++t) o = fmaf(fsh[t], o_part[(size_t(t) * DS4X_ATTN_HEADS + h) * DS4X_KV_DIM + d], o);
+    out[size_t(h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+  }
+  if (tid == 0 && lse != nullptr) lse[h] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+}  // namespace
+
+size_t dense_attn_ws_bytes(int64_t n_rows) { return dense_layout(n_rows < 1 ? 1 : n_rows).total; }
+
+cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
+                              float *lse, void *ws, cudaStream_t stream) {
+  const int64_t tiles = (n_rows + DS4X_TOPK_MAX - 1) / DS4X_TOPK_MAX;
+  if (n_rows < 1 || tiles > kDenseMaxTiles) return cudaErrorInvalidValue;
+  const DenseWsLayout L = dense_layout(n_rows);
+  char *base = static_cast<char *>(ws);
+  float *lse_part = reinterpret_cast<float *>(base + L.lse);
+  float *o_part = reinterpret_cast<float *>(base + L.o);
+  AttnBatch ab{};
+  ab.kv = kv_rows;
+  ab.n_rows = n_rows;
+  ab.k = DS4X_TOPK_MAX;
+  ab.scale = scale;
+  ab.q = q;
+  ab.q_shared = true;
+  ab.lse = lse_part;
+  ab.out_f32 = o_part;
+  cudaError_t e = launch_attn_items<true>(ab, int(tiles), ws, stream);
+  if (e != cudaSuccess) return e;
+  dense_finalize_kernel<<<DS4X_ATTN_HEADS, 256, size_t(tiles) * sizeof(float), stream>>>(lse_part, o_part, int(tiles),
+                                                                                         out, lse);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

@@ -137,9 +137,19 @@ struct AttnBatch {
   const uint16_t *q;
   uint16_t *out;
   float *lse;
+  bool q_shared;   // every item reads the one query at q (dense tiles)
+  float *out_f32;  // dense tiles: item b's normalised fp32 output at out_f32 + b * 64 * 512, not out
 };
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
 size_t attn_decode_ws_bytes(int32_t k);
+
+// Dense attention over every row [0, n_rows) (one query): 512-row tiles as
+// the items of one attention launch (fp32 partials), then a finalize.
+constexpr int64_t kDenseMaxTiles = 8192;  // rows up to 8192 * 512
+static_assert(kDenseMaxTiles * DS4X_TOPK_MAX == DS4X_DENSE_MAX_ROWS, "the ABI's row limit");
+size_t dense_attn_ws_bytes(int64_t n_rows);
+cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
+                              float *lse, void *ws, cudaStream_t stream);
 
 // Chunked prefill: query quantiser and the multi-query scorer.
 cudaError_t launch_quantize_query(const float *q, int64_t n_vec, uint8_t *codes, uint8_t *scales,

@@ -65,6 +65,7 @@ typedef struct CUstream_st *ds4x_stream_t;
 #define DS4X_TOPK_MAX 512
 #define DS4X_MAX_SESSIONS 64
 #define DS4X_PREFILL_MAX_QUERIES 65535
+#define DS4X_DENSE_MAX_ROWS (8192LL * 512)
 
 enum {
   DS4X_OK = 0,
@@ -333,6 +334,35 @@ int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32
 int ds4x_sparse_attn_decode_noalloc(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                     int32_t k, const uint16_t *q_bf16, float softmax_scale,
                                     uint16_t *out_bf16, float *lse, ds4x_stream_t stream);
+
+/* Dense decode attention over EVERY row of a KV row array: the HCA layers'
+ * exact attention over all their compressed rows (DS4X README, "Optimization
+ * details", the HCA bullet: exact score-split attention with no row
+ * ceiling).  For each head h < 64, over t in [0, n_rows):
+ *
+ *   l_ht = softmax_scale * (q_h . v_t),  o_h = sum_t softmax_t(l_ht) v_t,
+ *   lse_h = log sum_t e^(l_ht)
+ *
+ * with v_t the dequantised row as in ds4x_sparse_attn_decode.  Computed as
+ * 512-row tiles (each one attention item writing its normalised fp32 output
+ * and LSE into the workspace), then a log-sum-exp combine over the tiles.
+ *
+ *   kv_rows   u8 [n_rows][583]
+ *   n_rows    1 .. DS4X_DENSE_MAX_ROWS
+ *   q_bf16    u16 [64][512]
+ *   out_bf16  u16 [64][512] (bf16, round to nearest even)
+ *   lse       f32 [64] or NULL
+ *   ws        ds4x_dense_attn_decode_workspace(n_rows) bytes, owned by the
+ *             caller; no initialisation needed; its first 256 bytes are
+ *             the status header (ds4x_workspace_status)
+ *
+ * Errors: DS4X_EINVAL (null or misaligned pointer, n_rows out of range),
+ * DS4X_EWORKSPACE (ws_bytes too small), DS4X_EARCH, DS4X_ECUDA.
+ */
+size_t ds4x_dense_attn_decode_workspace(int64_t n_rows);
+int ds4x_dense_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q_bf16,
+                           float softmax_scale, uint16_t *out_bf16, float *lse, void *ws,
+                           size_t ws_bytes, ds4x_stream_t stream);
 
 #ifdef __cplusplus
 }

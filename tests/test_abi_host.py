@@ -133,3 +133,22 @@ def test_prefill_scorer_argument_checks(lib):
     assert g(FAKE, 65536, FAKE, FAKE, FAKE, 0, 63488, 512, FAKE, None, FAKE, ws, None) == -1
     assert g(FAKE, 65536, FAKE, FAKE, FAKE, 2048, 63488, 0, FAKE, None, FAKE, ws, None) == -1
     assert g(FAKE, 65536, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws - 1, None) == -3
+
+
+def test_dense_attention_argument_checks(lib):
+    s = ctypes.c_float(0.044)
+    wsz = lib.ds4x_dense_attn_decode_workspace
+    # header, tile LSEs (64 floats a tile, rounded up to 256 bytes), tile outputs (64 x 512 floats a tile)
+    for n, tiles in [(1, 1), (512, 1), (513, 2), (8192, 16), (100000, 196)]:
+        assert wsz(n) == 256 + ((tiles * 64 * 4 + 255) // 256) * 256 + tiles * 64 * 512 * 4, n
+    f = lib.ds4x_dense_attn_decode
+    ws = wsz(8192)
+    assert f(None, 8192, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 8192, None, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 8192, FAKE, s, None, None, FAKE, ws, None) == -1
+    assert f(FAKE, 8192, FAKE, s, FAKE, None, None, ws, None) == -1
+    assert f(FAKE, 0, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 8192 * 512 + 1, FAKE, s, FAKE, None, FAKE, 1 << 40, None) == -1  # beyond DS4X_DENSE_MAX_ROWS
+    assert f(FAKE + 4, 8192, FAKE, s, FAKE, None, FAKE, ws, None) == -1
+    assert f(FAKE, 8192, FAKE, s, FAKE, FAKE + 4, FAKE, ws, None) == -1
+    assert f(FAKE, 8192, FAKE, s, FAKE, None, FAKE, ws - 1, None) == -3
