@@ -87,3 +87,37 @@ def lse_combine(parts):
     tot = f.sum(axis=0)
     out = np.where(tot[:, None] > 0, (f[:, :, None] * o).sum(axis=0) / np.where(tot > 0, tot, 1.0)[:, None], 0.0)
     return out, np.where(tot > 0, safe_m + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+
+
+def window_sparse_attn_decode(kv_rows, idx, ring_rows, ring_pos, w: int, q_bf16, scale: float):
+    """Decode attention over the selected compressed rows AND the raw
+    sliding window: each layer keeps a raw KV ring of packed 583-byte rows,
+    padded to 256 rows (DS4X README, "Packed cache ABI"), whose live rows are
+    the most recent tokens; a checkpoint stores them in logical position
+    order rather than physical ring order (ds4 README, "Disk KV Cache").
+    Reading: one softmax over the union of the two row sets (equivalently
+    the log-sum-exp merge of the sparse and the window attention).
+
+    kv_rows   : uint8 [n, 583] compressed rows; idx: int [k] (-1 = skip)
+    ring_rows : uint8 [R, 583] the ring in physical order
+    ring_pos  : physical slot of the newest window row; the window is the w
+                slots ring_pos, ring_pos - 1, ... (mod R), 0 <= w <= R
+    Returns (out bf16-rounded, out_exact, lse) as sparse_attn_decode.
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    sel = np.asarray(kv_rows)[idx[idx >= 0]]
+    ring = np.asarray(ring_rows)
+    slots = (int(ring_pos) - np.arange(int(w))) % ring.shape[0] if w > 0 else np.zeros(0, dtype=np.int64)
+    rows = np.concatenate([sel, ring[slots]], axis=0) if (sel.shape[0] + slots.size) > 0 else sel
+    q = bf16_decode(q_bf16)
+    heads, dim = q.shape
+    if rows.shape[0] == 0:
+        zero = np.zeros((heads, dim))
+        return zero, zero, np.full(heads, -np.inf)
+    v = unpack_kv_rows(rows)
+    logits = float(scale) * (q @ v.T)
+    m = logits.max(axis=1)
+    e = np.exp(logits - m[:, None])
+    s = e.sum(axis=1)
+    out = (e @ v) / s[:, None]
+    return bf16_round(out), out, m + np.log(s)
