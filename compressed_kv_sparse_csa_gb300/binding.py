@@ -38,6 +38,9 @@ _SIGNATURES = {
     "ds4x_sparse_attn_decode_noalloc": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p]),
     "ds4x_dense_attn_decode_workspace": (_c_size, [_c_i64]),
     "ds4x_dense_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_f32, _c_p, _c_p, _c_p, _c_size, _c_p]),
+    "ds4x_window_sparse_attn_decode_workspace": (_c_size, []),
+    "ds4x_window_sparse_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_f32,
+                                                      _c_p, _c_p, _c_p, _c_size, _c_p]),
     "ds4x_index_score_topk_batched_workspace": (_c_size, [_c_i32, _c_i32]),
     "ds4x_index_score_topk_batched": (ctypes.c_int, [_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size,
                                                       _c_p]),
@@ -191,6 +194,26 @@ def ds4x_dense_attn_decode(kv_rows, n_rows, q_bf16, softmax_scale, out_bf16, lse
     _check(ws, torch.uint8, "ws")
     _call("ds4x_dense_attn_decode", _ptr(kv_rows), int(n_rows), _ptr(q_bf16), float(softmax_scale), _ptr(out_bf16),
           _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_window_sparse_attn_decode_workspace() -> int:
+    return lib().ds4x_window_sparse_attn_decode_workspace()
+
+
+def ds4x_window_sparse_attn_decode(kv_rows, n_rows, idx, k, ring_rows, ring_pos, w, q_bf16, softmax_scale, out_bf16,
+                                   lse, ws, stream=None):
+    """Decode attention of q_bf16 [64, 512] over the k rows listed in idx and
+    the raw window's w ring rows (slots ring_pos, ring_pos - 1, ... mod 256)."""
+    _check(kv_rows, torch.uint8, "kv_rows", numel=int(n_rows) * 583)
+    _check(idx, torch.int32, "idx", numel=int(k))
+    _check(ring_rows, torch.uint8, "ring_rows", numel=256 * 583)
+    _check(q_bf16, torch.bfloat16, "q_bf16", numel=64 * 512)
+    _check(out_bf16, torch.bfloat16, "out_bf16", numel=64 * 512)
+    _check(lse, torch.float32, "lse", numel=64, allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_window_sparse_attn_decode", _ptr(kv_rows), int(n_rows), _ptr(idx), int(k), _ptr(ring_rows),
+          int(ring_pos), int(w), _ptr(q_bf16), float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(),
+          _stream(stream))
 
 
 def ds4x_sparse_attn_decode_noalloc(kv_rows, n_rows, idx, k, q_bf16, softmax_scale, out_bf16, lse, stream=None):

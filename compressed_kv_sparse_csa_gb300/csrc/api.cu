@@ -252,6 +252,28 @@ int ds4x_dense_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const uint16_
   return from_cuda(launch_dense_attn(kv_rows, n_rows, q_bf16, softmax_scale, out_bf16, lse, ws, stream));
 }
 
+size_t ds4x_window_sparse_attn_decode_workspace(void) { return window_attn_ws_bytes(); }
+
+int ds4x_window_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t k,
+                                   const uint8_t *ring_rows, int32_t ring_pos, int32_t w, const uint16_t *q_bf16,
+                                   float softmax_scale, uint16_t *out_bf16, float *lse, void *ws, size_t ws_bytes,
+                                   ds4x_stream_t stream) {
+  if (kv_rows == nullptr || idx == nullptr || ring_rows == nullptr || q_bf16 == nullptr || out_bf16 == nullptr ||
+      ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(kv_rows) || !aligned16(idx) || !aligned16(ring_rows) || !aligned16(q_bf16) ||
+      !aligned16(out_bf16) || !aligned16(ws) || (lse != nullptr && !aligned16(lse)))
+    return DS4X_EINVAL;
+  if (n_rows < 1 || k < 1 || k > DS4X_TOPK_MAX || ring_pos < 0 || ring_pos >= DS4X_RING_ROWS || w < 0 ||
+      w > DS4X_RING_ROWS)
+    return DS4X_EINVAL;
+  if (ws_bytes < ds4x_window_sparse_attn_decode_workspace()) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  return from_cuda(launch_window_attn(kv_rows, n_rows, idx, k, ring_rows, ring_pos, w, q_bf16, softmax_scale,
+                                      out_bf16, lse, ws, stream));
+}
+
 int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, uint8_t *scales,
                               ds4x_stream_t stream) {
   if (q == nullptr || codes == nullptr || scales == nullptr) return DS4X_EINVAL;

@@ -194,7 +194,9 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   const float scale = ab.scale;
   const int32_t *__restrict__ idx = DENSE ? nullptr : ab.idx + size_t(bz) * k;
   const uint16_t *__restrict__ q = ab.q + (ab.q_shared ? size_t(0) : size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM);
-  uint16_t *__restrict__ out = DENSE ? nullptr : ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
+  // fp32 output (dense tiles, window + sparse items) for a finalize, else bf16
+  const bool f32_out = DENSE || ab.out_f32 != nullptr;
+  uint16_t *__restrict__ out = f32_out ? nullptr : ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
   float *__restrict__ lse = ab.lse != nullptr ? ab.lse + size_t(bz) * DS4X_ATTN_HEADS : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char *Kh = smem;                                   // [64][1040]: raw row, then fp16
@@ -575,7 +577,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
       of[v] = L > 0.f ? o / L : 0.f;
       ob[v] = __bfloat16_as_ushort(__float2bfloat16_rn(of[v]));
     }
-    if (DENSE) {  // the tile's normalised output in fp32, for the finalize
+    if (f32_out) {  // the item's normalised output in fp32, for the finalize
       float *fdst = ab.out_f32 + (size_t(bz) * DS4X_ATTN_HEADS + size_t(hg * HG + h)) * DS4X_KV_DIM + d;
       if (kV == 4) {
         *reinterpret_cast<float4 *>(fdst) = make_float4(of[0], of[kV > 1 ? 1 : 0], of[kV > 2 ? 2 : 0], of[kV > 3 ? 3 : 0]);
@@ -704,6 +706,77 @@ __global__ void __launch_bounds__(256) dense_finalize_kernel(const float *__rest
 }  // namespace
 
 size_t dense_attn_ws_bytes(int64_t n_rows) { return dense_layout(n_rows < 1 ? 1 : n_rows).total; }
+
+namespace {
+
+// The window + sparse attention's workspace: the status header, the two
+// items' LSEs [2][64] and normalised outputs [2][64][512] (fp32), their index
+// lists [2][512], row-array pointers [2] and row counts [2].
+struct WindowWsLayout {
+  size_t lse, o, idx, ptrs, lens, total;
+};
+constexpr WindowWsLayout window_layout() {
+  WindowWsLayout L{};
+  L.lse = kWsHeaderBytes;
+  L.o = L.lse + 2 * DS4X_ATTN_HEADS * sizeof(float);
+  L.idx = L.o + size_t(2) * DS4X_ATTN_HEADS * DS4X_KV_DIM * sizeof(float);
+  L.ptrs = L.idx + 2 * DS4X_TOPK_MAX * sizeof(int32_t);
+  L.lens = L.ptrs + 2 * sizeof(void *);
+  L.total = L.lens + 2 * sizeof(int64_t);
+  return L;
+}
+
+// Item 0: the caller's k selected rows; item 1: the window, ring slots
+// ring_pos, ring_pos - 1, ... (mod DS4X_RING_ROWS), w of them.
+__global__ void __launch_bounds__(DS4X_TOPK_MAX) window_prep_kernel(const uint8_t *kv_rows, int64_t n_rows,
+                                                                    const int32_t *__restrict__ idx, int32_t k,
+                                                                    const uint8_t *ring_rows, int32_t ring_pos,
+                                                                    int32_t w, int32_t *__restrict__ idx2,
+                                                                    const uint8_t **ptrs, int64_t *lens) {
+  const int j = threadIdx.x;
+  idx2[j] = j < k ? idx[j] : -1;
+  idx2[DS4X_TOPK_MAX + j] = j < w ? (ring_pos - j + DS4X_RING_ROWS) % DS4X_RING_ROWS : -1;
+  if (j == 0) {
+    ptrs[0] = kv_rows;
+    ptrs[1] = ring_rows;
+    lens[0] = n_rows;
+    lens[1] = DS4X_RING_ROWS;
+  }
+}
+
+}  // namespace
+
+size_t window_attn_ws_bytes() { return window_layout().total; }
+
+cudaError_t launch_window_attn(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t k,
+                               const uint8_t *ring_rows, int32_t ring_pos, int32_t w, const uint16_t *q, float scale,
+                               uint16_t *out, float *lse, void *ws, cudaStream_t stream) {
+  constexpr WindowWsLayout L = window_layout();
+  char *base = static_cast<char *>(ws);
+  float *lse_part = reinterpret_cast<float *>(base + L.lse);
+  float *o_part = reinterpret_cast<float *>(base + L.o);
+  int32_t *idx2 = reinterpret_cast<int32_t *>(base + L.idx);
+  const uint8_t **ptrs = reinterpret_cast<const uint8_t **>(base + L.ptrs);
+  int64_t *lens = reinterpret_cast<int64_t *>(base + L.lens);
+  window_prep_kernel<<<1, DS4X_TOPK_MAX, 0, stream>>>(kv_rows, n_rows, idx, k, ring_rows, ring_pos, w, idx2, ptrs,
+                                                      lens);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  AttnBatch ab{};
+  ab.kv_arr = ptrs;
+  ab.n_arr = lens;
+  ab.idx = idx2;
+  ab.k = DS4X_TOPK_MAX;
+  ab.scale = scale;
+  ab.q = q;
+  ab.q_shared = true;
+  ab.lse = lse_part;
+  ab.out_f32 = o_part;
+  e = launch_attn_items<false>(ab, 2, ws, stream);
+  if (e != cudaSuccess) return e;
+  dense_finalize_kernel<<<DS4X_ATTN_HEADS, 256, 2 * sizeof(float), stream>>>(lse_part, o_part, 2, out, lse);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
                               float *lse, void *ws, cudaStream_t stream) {

@@ -138,7 +138,7 @@ struct AttnBatch {
   uint16_t *out;
   float *lse;
   bool q_shared;   // every item reads the one query at q (dense tiles)
-  float *out_f32;  // dense tiles: item b's normalised fp32 output at out_f32 + b * 64 * 512, not out
+  float *out_f32;  // item b's normalised fp32 output at out_f32 + b * 64 * 512 instead of out (for a finalize)
 };
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
 size_t attn_decode_ws_bytes(int32_t k);
@@ -150,6 +150,14 @@ static_assert(kDenseMaxTiles * DS4X_TOPK_MAX == DS4X_DENSE_MAX_ROWS, "the ABI's 
 size_t dense_attn_ws_bytes(int64_t n_rows);
 cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
                               float *lse, void *ws, cudaStream_t stream);
+
+// Attention over k selected rows plus the raw sliding window's w ring rows
+// (one softmax over both): the two as items of one attention launch (fp32
+// partials), then the finalize.
+size_t window_attn_ws_bytes();
+cudaError_t launch_window_attn(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t k,
+                               const uint8_t *ring_rows, int32_t ring_pos, int32_t w, const uint16_t *q, float scale,
+                               uint16_t *out, float *lse, void *ws, cudaStream_t stream);
 
 // Chunked prefill: query quantiser and the multi-query scorer.
 cudaError_t launch_quantize_query(const float *q, int64_t n_vec, uint8_t *codes, uint8_t *scales,

@@ -66,6 +66,7 @@ typedef struct CUstream_st *ds4x_stream_t;
 #define DS4X_MAX_SESSIONS 64
 #define DS4X_PREFILL_MAX_QUERIES 65535
 #define DS4X_DENSE_MAX_ROWS (8192LL * 512)
+#define DS4X_RING_ROWS 256
 
 enum {
   DS4X_OK = 0,
@@ -360,6 +361,34 @@ int ds4x_sparse_attn_decode_noalloc(const uint8_t *kv_rows, int64_t n_rows, cons
  * DS4X_EWORKSPACE (ws_bytes too small), DS4X_EARCH, DS4X_ECUDA.
  */
 size_t ds4x_dense_attn_decode_workspace(int64_t n_rows);
+
+/* Decode attention over k selected compressed rows AND the raw sliding
+ * window: each layer keeps a raw KV ring of DS4X_RING_ROWS packed 583-byte
+ * rows (DS4X README, "Packed cache ABI": the raw ring padded to 256 rows),
+ * whose live rows are the most recent tokens.  One softmax over the union of
+ * the two row sets (no deduplication), i.e. the log-sum-exp merge of the
+ * sparse and the window attention:
+ *
+ *   rows = { kv_rows[idx[j]] : j < k, idx[j] >= 0 }
+ *        + { ring_rows[(ring_pos - j) mod 256] : j < w }
+ *
+ *   kv_rows, n_rows, idx, k      as ds4x_sparse_attn_decode (1 <= k <= 512)
+ *   ring_rows u8 [DS4X_RING_ROWS][583], physical ring order
+ *   ring_pos  the newest window row's slot, 0 .. 255
+ *   w         live window rows, 0 .. 256
+ *   q_bf16, softmax_scale, out_bf16, lse   as ds4x_sparse_attn_decode
+ *   ws        ds4x_window_sparse_attn_decode_workspace() bytes; its first
+ *             256 bytes are the status header (an index outside
+ *             [-1, n_rows) is skipped and flags DS4X_EDEVICE there)
+ *
+ * Errors: DS4X_EINVAL (null or misaligned pointer, k, ring_pos or w out of
+ * range), DS4X_EWORKSPACE, DS4X_EARCH, DS4X_ECUDA.
+ */
+size_t ds4x_window_sparse_attn_decode_workspace(void);
+int ds4x_window_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t k,
+                                   const uint8_t *ring_rows, int32_t ring_pos, int32_t w,
+                                   const uint16_t *q_bf16, float softmax_scale, uint16_t *out_bf16,
+                                   float *lse, void *ws, size_t ws_bytes, ds4x_stream_t stream);
 int ds4x_dense_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q_bf16,
                            float softmax_scale, uint16_t *out_bf16, float *lse, void *ws,
                            size_t ws_bytes, ds4x_stream_t stream);

@@ -152,3 +152,28 @@ def test_dense_attention_argument_checks(lib):
     assert f(FAKE + 4, 8192, FAKE, s, FAKE, None, FAKE, ws, None) == -1
     assert f(FAKE, 8192, FAKE, s, FAKE, FAKE + 4, FAKE, ws, None) == -1
     assert f(FAKE, 8192, FAKE, s, FAKE, None, FAKE, ws - 1, None) == -3
+
+
+def test_window_attention_argument_checks(lib):
+    s = ctypes.c_float(0.044)
+    ws = lib.ds4x_window_sparse_attn_decode_workspace()
+    # header, two items' LSEs and fp32 outputs, two index lists, two row pointers and lengths
+    assert ws == 256 + 2 * 64 * 4 + 2 * 64 * 512 * 4 + 2 * 512 * 4 + 16 + 16
+    f = lib.ds4x_window_sparse_attn_decode
+    ok = (FAKE, 1000, FAKE, 512, FAKE, 10, 20, FAKE, s, FAKE, None, FAKE, ws, None)
+
+    def call(**kw):
+        names = ["kv", "n", "idx", "k", "ring", "pos", "w", "q", "scale", "out", "lse", "ws", "wsb", "stream"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return f(*[args[n] for n in names])
+
+    for key in ("kv", "idx", "ring", "q", "out", "ws"):
+        assert call(**{key: None}) == -1, key
+    assert call(ring=FAKE + 4) == -1
+    assert call(lse=FAKE + 4) == -1
+    assert call(n=0) == -1
+    assert call(k=0) == -1 and call(k=513) == -1
+    assert call(pos=-1) == -1 and call(pos=256) == -1
+    assert call(w=-1) == -1 and call(w=257) == -1
+    assert call(wsb=ws - 1) == -3
