@@ -177,3 +177,12 @@ def test_window_attention_argument_checks(lib):
     assert call(pos=-1) == -1 and call(pos=256) == -1
     assert call(w=-1) == -1 and call(w=257) == -1
     assert call(wsb=ws - 1) == -3
+
+
+def test_ring_rows_match_the_pages_allocation():
+    """DS4X_RING_ROWS: the raw ring the pages' allocation example counts,
+    43 layers x 256 rows x 583 bytes = the printed raw-ring bytes."""
+    g = golden("packed_cache_abi.txt")
+    text = open(HEADER).read()
+    ring = int(re.search(r"#define DS4X_RING_ROWS (\d+)", text).group(1))
+    assert 43 * ring * int(g["kv_row_bytes"]) == int(g["alloc_raw_rings"])
