@@ -39,6 +39,10 @@ _SIGNATURES = {
     "ds4x_dense_attn_decode_workspace": (_c_size, [_c_i64]),
     "ds4x_dense_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_f32, _c_p, _c_p, _c_p, _c_size, _c_p]),
     "ds4x_window_sparse_attn_decode_workspace": (_c_size, []),
+    "ds4x_checkpoint_bytes": (_c_i64, [_c_p, _c_i32]),
+    "ds4x_checkpoint_save": (ctypes.c_int, [_c_p, _c_i32, _c_p, _c_i64]),
+    "ds4x_checkpoint_inspect": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_i32]),
+    "ds4x_checkpoint_load": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32]),
     "ds4x_window_sparse_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_f32,
                                                       _c_p, _c_p, _c_p, _c_size, _c_p]),
     "ds4x_index_score_topk_batched_workspace": (_c_size, [_c_i32, _c_i32]),
@@ -214,6 +218,76 @@ def ds4x_window_sparse_attn_decode(kv_rows, n_rows, idx, k, ring_rows, ring_pos,
     _call("ds4x_window_sparse_attn_decode", _ptr(kv_rows), int(n_rows), _ptr(idx), int(k), _ptr(ring_rows),
           int(ring_pos), int(w), _ptr(q_bf16), float(softmax_scale), _ptr(out_bf16), _ptr(lse), _ptr(ws), ws.numel(),
           _stream(stream))
+
+
+# ---- packed-row checkpoints: host memory (numpy uint8 arrays and bytes) ----
+
+class _LayerRows(ctypes.Structure):
+    _fields_ = [("ratio", _c_i32), ("ring_live", _c_i32), ("ring_pos", _c_i32), ("reserved", _c_i32),
+                ("ring_rows", _c_p), ("kv_rows", _c_p), ("idx_rows", _c_p), ("n_kv", _c_i64), ("n_idx", _c_i64)]
+
+
+class _LayerCounts(ctypes.Structure):
+    _fields_ = [("ratio", _c_i32), ("ring_live", _c_i32), ("n_kv", _c_i64), ("n_idx", _c_i64)]
+
+
+class _LayerBuffers(ctypes.Structure):
+    _fields_ = [("ring_rows", _c_p), ("kv_rows", _c_p), ("idx_rows", _c_p), ("kv_cap", _c_i64), ("idx_cap", _c_i64)]
+
+
+def _np_ptr(a):
+    import numpy as np
+
+    if a is None:
+        return None
+    if not (isinstance(a, np.ndarray) and a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"]):
+        raise ValueError("checkpoint rows must be contiguous numpy uint8 arrays")
+    return a.ctypes.data
+
+
+def _layer_rows(layers):
+    arr = (_LayerRows * max(1, len(layers)))()
+    for i, L in enumerate(layers):
+        kv, ix = L.get("kv_rows"), L.get("idx_rows")
+        arr[i] = _LayerRows(int(L["ratio"]), int(L.get("ring_live", 0)), int(L.get("ring_pos", 0)), 0,
+                            _np_ptr(L.get("ring_rows")), _np_ptr(kv), _np_ptr(ix),
+                            0 if kv is None else kv.size // 583, 0 if ix is None else ix.size // 68)
+    return arr
+
+
+def ds4x_checkpoint_save(layers) -> bytes:
+    """layers: dicts with ratio, ring_live, ring_pos, ring_rows (uint8 [256 * 583],
+    physical order), kv_rows (uint8 [n * 583]) and idx_rows (uint8 [n * 68])."""
+    arr = _layer_rows(layers)
+    nbytes = lib().ds4x_checkpoint_bytes(ctypes.addressof(arr), len(layers))
+    if nbytes < 0:
+        raise Ds4xError("ds4x_checkpoint_bytes", int(nbytes))
+    out = ctypes.create_string_buffer(int(nbytes))
+    _call("ds4x_checkpoint_save", ctypes.addressof(arr), len(layers), ctypes.addressof(out), int(nbytes))
+    return out.raw
+
+
+def ds4x_checkpoint_inspect(data: bytes):
+    """The layer counts of a checkpoint (raises Ds4xError for a bad one)."""
+    n = _c_i32(0)
+    buf = ctypes.create_string_buffer(bytes(data), len(data))
+    _call("ds4x_checkpoint_inspect", ctypes.addressof(buf), len(data), ctypes.byref(n), None, 0)
+    counts = (_LayerCounts * max(1, n.value))()
+    _call("ds4x_checkpoint_inspect", ctypes.addressof(buf), len(data), ctypes.byref(n), ctypes.addressof(counts),
+          n.value)
+    return [{"ratio": c.ratio, "ring_live": c.ring_live, "n_kv": c.n_kv, "n_idx": c.n_idx} for c in counts[:n.value]]
+
+
+def ds4x_checkpoint_load(data: bytes, bufs):
+    """Loads into bufs: dicts with ring_rows (uint8 [256 * 583]), kv_rows and
+    idx_rows (uint8, their capacity in rows from their size)."""
+    arr = (_LayerBuffers * max(1, len(bufs)))()
+    for i, b in enumerate(bufs):
+        kv, ix = b.get("kv_rows"), b.get("idx_rows")
+        arr[i] = _LayerBuffers(_np_ptr(b.get("ring_rows")), _np_ptr(kv), _np_ptr(ix),
+                               0 if kv is None else kv.size // 583, 0 if ix is None else ix.size // 68)
+    buf = ctypes.create_string_buffer(bytes(data), len(data))
+    _call("ds4x_checkpoint_load", ctypes.addressof(buf), len(data), ctypes.addressof(arr), len(bufs))
 
 
 def ds4x_sparse_attn_decode_noalloc(kv_rows, n_rows, idx, k, q_bf16, softmax_scale, out_bf16, lse, stream=None):

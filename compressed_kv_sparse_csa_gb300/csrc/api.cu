@@ -59,6 +59,8 @@ const char *ds4x_status_str(int status) {
     case DS4X_ECUDA: return "CUDA runtime error";
     case DS4X_ETIMEOUT: return "bounded device wait gave up";
     case DS4X_EDEVICE: return "kernel-detected invalid input (index out of range)";
+    case DS4X_EFORMAT: return "not a checkpoint of this layout, or corrupt or truncated";
+    case DS4X_EVERSION: return "a checkpoint of another payload version";
     default: return "unknown status";
   }
 }

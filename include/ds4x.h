@@ -67,6 +67,7 @@ typedef struct CUstream_st *ds4x_stream_t;
 #define DS4X_PREFILL_MAX_QUERIES 65535
 #define DS4X_DENSE_MAX_ROWS (8192LL * 512)
 #define DS4X_RING_ROWS 256
+#define DS4X_CHECKPOINT_MAX_LAYERS 4096
 
 enum {
   DS4X_OK = 0,
@@ -76,7 +77,9 @@ enum {
   DS4X_EARCH = -4,      /* current device is not compute capability 10.3   */
   DS4X_ECUDA = -5,      /* a CUDA runtime call or launch failed            */
   DS4X_ETIMEOUT = -6,   /* device status: a bounded wait gave up           */
-  DS4X_EDEVICE = -7     /* device status: kernel-detected bad input        */
+  DS4X_EDEVICE = -7,    /* device status: kernel-detected bad input        */
+  DS4X_EFORMAT = -8,    /* not a checkpoint of this layout, or corrupt     */
+  DS4X_EVERSION = -9    /* a checkpoint of another payload version         */
 };
 
 /* Static text for a status code (host pointer, never NULL). */
@@ -392,6 +395,71 @@ int ds4x_window_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const
 int ds4x_dense_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q_bf16,
                            float softmax_scale, uint16_t *out_bf16, float *lse, void *ws,
                            size_t ws_bytes, ds4x_stream_t stream);
+
+/* ---- Packed-row checkpoints (host memory, no CUDA call) -----------------
+ *
+ * A checkpoint holds, per layer, the native packed rows: the raw sliding
+ * window's live rows, the compressed KV rows and (CSA layers) the indexer
+ * rows.  Disk checkpoints store the packed rows and the payload version (3)
+ * rejects payloads of any other version, such as F32-cache version 2 (DS4X
+ * README, "Optimization details"); the window rows go in logical position
+ * order, oldest first, not physical ring order (ds4 README, "Disk KV Cache").
+ * Tokens, logits and the compressor's frontier tensors are model state and
+ * are not part of it.
+ *
+ * Layout (little-endian; this library's own):
+ *   header, 64 bytes: "DS4X", u32 payload version = 3, u32 header bytes =
+ *     64, u32 layer count, u32 ring rows = 256, u32 KV row bytes = 583,
+ *     u32 indexer row bytes = 68, u32 layer entry bytes = 32, u64 total
+ *     bytes, 24 zero bytes
+ *   one 32-byte entry per layer: u32 ratio (0: raw window only; 4: CSA, KV
+ *     and as many indexer rows; 128: HCA, KV rows), u32 live window rows
+ *     (0..256), u64 KV rows, u64 indexer rows, u64 zero
+ *   then per layer, in order: the live window rows (583 B each, oldest
+ *     first), the KV rows (583 B each), the indexer rows (68 B each)
+ *
+ * All pointers here are host pointers, any alignment.  A file is checked
+ * whole (magic, version, sizes, every entry, the total) before any row is
+ * read: DS4X_EFORMAT for anything that is not this layout or is truncated,
+ * DS4X_EVERSION for another payload version.
+ */
+typedef struct ds4x_layer_rows {
+  int32_t ratio;              /* 0, 4 or 128 */
+  int32_t ring_live;          /* live window rows, 0..DS4X_RING_ROWS */
+  int32_t ring_pos;           /* the newest window row's slot, 0..255 */
+  int32_t reserved;
+  const uint8_t *ring_rows;   /* [DS4X_RING_ROWS][583], physical ring order */
+  const uint8_t *kv_rows;     /* [n_kv][583] */
+  const uint8_t *idx_rows;    /* [n_idx][68], CSA layers only */
+  int64_t n_kv, n_idx;        /* CSA: n_idx == n_kv; HCA: n_idx == 0; ratio 0: both 0 */
+} ds4x_layer_rows;
+
+typedef struct ds4x_layer_counts {
+  int32_t ratio, ring_live;
+  int64_t n_kv, n_idx;
+} ds4x_layer_counts;
+
+typedef struct ds4x_layer_buffers {
+  uint8_t *ring_rows;         /* [DS4X_RING_ROWS][583]: the window lands in slots
+                                 0..ring_live-1, oldest first (newest slot ring_live-1) */
+  uint8_t *kv_rows;           /* room for kv_cap rows */
+  uint8_t *idx_rows;          /* room for idx_cap rows */
+  int64_t kv_cap, idx_cap;
+} ds4x_layer_buffers;
+
+/* Bytes of the checkpoint of n_layers layers (0..DS4X_CHECKPOINT_MAX_LAYERS),
+ * or DS4X_EINVAL for an inconsistent layer (counts, ratio, null rows). */
+int64_t ds4x_checkpoint_bytes(const ds4x_layer_rows *layers, int32_t n_layers);
+/* Writes the checkpoint into dst (DS4X_ERANGE if dst_bytes is too small). */
+int ds4x_checkpoint_save(const ds4x_layer_rows *layers, int32_t n_layers, uint8_t *dst, int64_t dst_bytes);
+/* Checks src whole; gives its layer count and, if counts is not NULL (room
+ * for counts_cap layers, else DS4X_ERANGE), each layer's counts. */
+int ds4x_checkpoint_inspect(const uint8_t *src, int64_t src_bytes, int32_t *n_layers, ds4x_layer_counts *counts,
+                            int32_t counts_cap);
+/* Checks src whole and every destination (DS4X_EINVAL for n_layers other
+ * than the file's or a missing buffer, DS4X_ERANGE for too little room)
+ * before copying the rows. */
+int ds4x_checkpoint_load(const uint8_t *src, int64_t src_bytes, const ds4x_layer_buffers *bufs, int32_t n_layers);
 
 #ifdef __cplusplus
 }
