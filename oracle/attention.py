@@ -72,8 +72,8 @@ def dense_attn_decode(kv_rows, n: int, q_bf16, scale: float):
 
 
 def lse_combine(parts):
-    """The split-KV log-sum-exp combine (the benchmark spec's split-KV
-    flash-decoding; DS4X README, "Nsight Systems", the score-split finalize):
+    """The split-KV log-sum-exp combine of split-KV flash decoding (DS4X
+    README, "Nsight Systems": the score-split finalize kernel group):
     parts is a list of (o_s [H, D] normalised within split s, lse_s [H]); an
     empty split has lse -inf.  Returns (o, lse) with
         M = max_s lse_s,  o = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M),
