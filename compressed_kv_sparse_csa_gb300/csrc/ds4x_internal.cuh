@@ -18,7 +18,9 @@ struct WsHeader {
   int32_t status;        // DS4X_OK / DS4X_EDEVICE / DS4X_ETIMEOUT (sticky)
   uint32_t ticket;       // arrival counter of the fused scorer (self-resetting)
   uint32_t fallback;     // number of scorer calls that took the slow merge
-  uint32_t pad[61];
+  uint32_t wait_extra;   // arrivals the scorer's exchange waits for beyond its CTAs (0; a
+                         // nonzero value makes the bounded wait run out: the time-out test)
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 constexpr size_t kWsHeaderBytes = 256;

@@ -1064,7 +1064,8 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           }
           red_release_add(&ss.main[par], 1ull << 32);
           unsigned long long seen = 0ull;
-          const bool ok = wait_arrivals(&ss.main[par], unsigned(Gs), hdr, &seen);
+          const unsigned extra = __ldcg(&hdr->wait_extra);
+          const bool ok = wait_arrivals(&ss.main[par], unsigned(Gs) + extra, hdr, &seen);
           if (ok && int(blockIdx.x) == cta0) ss.epoch = sm.epoch + 1u;
           sm.sel.n_all = int(uint32_t(seen));
           sm.sel.ok = ok ? 1 : 0;

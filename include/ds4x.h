@@ -105,6 +105,14 @@ int64_t ds4x_cache_bytes(int64_t context_tokens);
  * otherwise; each call leaves it ready for the next call on the same
  * stream.  One workspace must not be used by two calls that may overlap on
  * the GPU.
+ *
+ * Bytes 12..15 of a scorer workspace (ds4x_index_score_topk and its batched
+ * and prefill forms) hold a u32: the arrivals its CTA exchange waits for
+ * beyond the CTAs of the session.  It is 0 in normal use.  A nonzero value
+ * makes the exchange's bounded wait run out (every CTA gives up after 0.5 s,
+ * writes no output and sets DS4X_ETIMEOUT): it exists to test the time-out
+ * path.  After a call that set DS4X_ETIMEOUT the workspace must be
+ * zero-filled again before its next use.
  */
 int ds4x_workspace_init(void *ws, size_t ws_bytes, ds4x_stream_t stream);
 
@@ -328,7 +336,10 @@ int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32
  * library holds that array until the process exits.  The call allocates
  * nothing and calls no allocating routine.  Its first call on a device looks
  * up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture.  All calls share
+ * current); make that first call before any stream capture.  The address is
+ * kept for the life of the process, so the call must not be used on a
+ * device after cudaDeviceReset has destroyed the context that first looked
+ * it up (the reloaded module may place the array elsewhere).  All calls share
  * the one array, so calls that may overlap on the GPU (different streams, or
  * several host threads) race and must be serialised by the caller.  Nothing
  * in the array needs to start at zero; out-of-range indices are skipped as

@@ -17,7 +17,9 @@ Named workloads: tiny decode N = 4096 (seed 1000), mid decode N = 131072
 (seed 1001), long decode N = 1048576 (seed 1002), 16 ragged sessions with
 lengths uniform on [8192, 65536] (seed 1003, lengths drawn first, then each
 session's arrays in the order above), chunked prefill of 2048 queries over
-65536 rows (seed 1004).  bfloat16 values are carried as uint16 bit patterns.
+65536 rows (seed 1004); indexer-only cases (keys, query, weights, in that
+order) for scorer checks beyond the long workload.  bfloat16 values are
+carried as uint16 bit patterns.
 """
 
 from __future__ import annotations
@@ -74,6 +76,17 @@ def decode_case(n: int, seed: int) -> dict:
     idx_in, kv_in = _draw_rows(rng, n)
     q_idx, w, q_attn = _draw_decode_query(rng)
     return {"n": n, "idx_in": idx_in, "kv_in": kv_in, "q_idx": q_idx, "w": w, "q_attn": q_attn}
+
+
+def indexer_case(n: int, seed: int) -> dict:
+    """Only the indexer side of a decode layer with n compressed rows (keys,
+    query, head weights; same distributions as ``decode_case``), for cases
+    too large to draw KV rows for."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    idx_in = _normal(rng, (n, IDX_DIM))
+    q_idx = to_bf16_bits(_normal(rng, (IDX_HEADS, IDX_DIM)))
+    w = (rng.random(IDX_HEADS, dtype=np.float32) / np.float32(8.0)).astype(np.float32)
+    return {"n": n, "idx_in": idx_in, "q_idx": q_idx, "w": w}
 
 
 def workload(name: str) -> dict:

@@ -54,14 +54,22 @@ def pack(idx_in=None, kv_in=None, capacity=None, chunks=1):
     return idx_rows, kv_rows
 
 
-def score_topk(idx_rows, n, q_bits, w, k=512):
+def score_topk(idx_rows, n, q_bits, w, k=512, return_ws=False):
     B = require_gpu()
     ws = new_ws(B.ds4x_index_score_topk_workspace(n, k))
     out_idx = torch.empty(k, dtype=torch.int32, device="cuda")
     out_score = torch.empty(k, dtype=torch.float32, device="cuda")
     B.ds4x_index_score_topk(idx_rows, n, bf16_dev(q_bits), dev(w), k, out_idx, out_score, ws)
     torch.cuda.synchronize()
+    if return_ws:
+        return out_idx.cpu().numpy(), out_score.cpu().numpy(), ws
     return out_idx.cpu().numpy(), out_score.cpu().numpy()
+
+
+def fallback_merges(ws):
+    """Scorer calls on this workspace that took the exact fallback merge
+    (the u32 at bytes 8..11 of the workspace header)."""
+    return int(ws[8:12].view(torch.int32).item())
 
 
 def attention(kv_rows, n, idx, q_bits, scale, ws=None):

@@ -29,6 +29,31 @@ def test_query_quantiser_matches_torch_e4m3():
     assert np.all(amax <= 448.0 * 2.0 ** e) and np.all(amax > 224.0 * 2.0 ** e)
 
 
+def test_query_dequantiser_matches_torch_e4m3_times_scale():
+    """Each 32-value block decodes as torch's float8_e4m3fn value of the code
+    times 2**(scale byte - 127), block b = elements 32b..32b+31 (so a wrong
+    scale axis, block width or code order fails here, independently of the
+    quantiser it usually feeds)."""
+    rng = np.random.default_rng(21)
+    codes = rng.integers(0, 256, size=(7, 64, 128), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scales = rng.integers(100, 155, size=(7, 64, 4), dtype=np.uint8)
+    # special blocks: every finite code once, extreme and unit scales, a constant block
+    codes[0, 0, :126] = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)[:126]
+    codes[0, 1, :] = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)[126:254]
+    scales[0, 0] = [1, 127, 200, 254]
+    scales[0, 1] = [127, 0, 127, 250]
+    codes[1, 2, 64:96] = 0x38  # 1.0 in E4M3
+    scales[1, 2, 2] = 130
+    got = P.dequantize_query_e4m3(codes, scales)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    factor = np.repeat(2.0 ** (scales.astype(np.float64) - 127.0), 32, axis=-1)
+    ref = dec * factor
+    assert got.shape == (7, 64, 128)
+    assert np.array_equal(got, ref)
+    assert np.all(got[1, 2, 64:96] == 8.0)
+
+
 def test_prefill_scores_causal_and_consistent_with_decode():
     case = prefill_case(T=6, n=300, causal_base=290)
     rows = C.pack_idx_rows(case["idx_in"])

@@ -48,7 +48,7 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         np.testing.assert_allclose(got_lse, ref_lse, rtol=1e-6, atol=1e-6)
 
 
-def test_noalloc_rejects_k_beyond_its_scratch():
+def test_noalloc_rejects_k_above_512():
     import torch
 
     B = require_gpu()
