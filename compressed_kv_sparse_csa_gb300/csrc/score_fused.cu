@@ -6,27 +6,34 @@
 // are merged into the exact top-512 without materialising the score array.
 // This is a GB300 design of that method.  One persistent CTA per SM:
 //
-//  * warp 16 streams the CTA's contiguous range of 128-row tiles (8,704 bytes
-//    each) from HBM with 1-D bulk copies into a ring of shared-memory stages;
-//  * converter warpgroups 0-1 (thread = row) move a tile into tensor memory as
-//    the MMA's A operand: each E2M1 code gets its own byte (code in bits 5-2,
-//    four codes per 32-bit column, 32 columns per row; a shift, a mask and a
-//    byte permute per eight codes), and the row's four UE8M0 bytes go to the
-//    row's scale-factor column (six-slot ring);
-//  * warps 17-19 (tile i by warp 17 + i % 3; a thread that waits on an
+//  * warp 20 streams the CTA's contiguous range of 128-row tiles from HBM,
+//    two tiles (17,408 bytes) per 1-D bulk copy, into a ring of five
+//    shared-memory stages (fewer, larger copies keep the copy engine near the
+//    HBM rate);
+//  * converter warpgroups 0-1 (tile i: warpgroup i % 2, thread = row) move a
+//    tile into tensor memory as the MMA's A operand: each E2M1 code gets its
+//    own byte in bits 5-2 (the container is read as bits 5-0; bits 7-6 are
+//    ignored), the even codes of each group of eight in one 32-bit column and
+//    the odd ones in the next (a mask and a shift per column; the query
+//    pieces are stored in the same K order), and the row's four UE8M0 bytes
+//    go to the row's scale-factor column (four-slot ring);
+//  * warps 21-23 (tile i by warp 21 + i % 3; a thread that waits on an
 //    mbarrier stalls until its own MMAs drain, so three issuers keep the
-//    tensor core fed)
-//    issue the tile's eight block-scaled tcgen05.mma kind::mxf8f6f4 (M = 128
-//    rows, N = 64 heads, K = 32; A = E2M1 keys with their own UE8M0 scales,
-//    B = one of the query's two E4M3 pieces with its UE8M0 scales per 32
-//    elements; both pieces accumulate into the same fp32 accumulator slot of
-//    a four-slot tensor-memory ring), so the hardware applies both sets of
-//    block scales and every row's 64 dot products come out in fp32;
-//  * epilogue warpgroups 2-3 read a row's 64 accumulators back and form
-//    s = sum_h w_h * ReLU(acc_h) (one max and one FMA per head); each key
-//    goes into shared memory and into a fixed 8,192-bucket histogram of its
-//    score bits;
-//  * after the stream one scan of the histogram locates the CTA's 512th and
+//    tensor core fed) issue the tile's eight block-scaled tcgen05.mma
+//    kind::mxf8f6f4 (M = 128 rows, N = 64 heads, K = 32; A = E2M1 keys with
+//    their own UE8M0 scales, B = one of the query's two E4M3 pieces with its
+//    UE8M0 scales per 32 elements; both pieces accumulate into the same fp32
+//    accumulator slot of a five-slot tensor-memory ring), so the hardware
+//    applies both sets of block scales and every row's 64 dot products come
+//    out in fp32;
+//  * epilogue warpgroups 2-4 (tile i: warpgroup 2 + i % 3) read a row's 64
+//    accumulators back and form s = sum_h w_h * ReLU(acc_h) (one max and one
+//    FMA per head); each key goes into shared memory and into a fixed
+//    8,192-bucket histogram of its score bits;
+//  * the rings' mbarriers are indexed by tile modulo a multiple of both the
+//    ring size and the waiters' rotation, so every waiter waits on every
+//    phase of its barriers;
+//  * after the stream (threads 0-511) one scan of the histogram locates the CTA's 512th and
 //    16th keys; one pass keeps the keys at or above the 512th key's bucket
 //    (a superset of the local top-512) and collects the keys at or above the
 //    16th key's bucket: the CTA's candidates, published unsorted with a
@@ -59,16 +66,24 @@ using namespace ptx;
 
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * DS4X_IDX_ROW_BYTES;  // 8704
-constexpr int kStages = 10;
-constexpr int kConvWG = 2;                 // converter warpgroups: warps 0-7
-constexpr int kEpiWG = 2;                  // epilogue warpgroups: warps 8-15
-constexpr int kWGThreads = 128 * (kConvWG + kEpiWG);  // 512
-constexpr int kProducerWarp = kWGThreads / 32;        // 16
-constexpr int kMmaWarp = kProducerWarp + 1;           // 17: allocates tensor memory; 17-19 issue MMAs
-constexpr int kMmaWarps = 3;                          // tile i is issued by warp kMmaWarp + i % 3
-constexpr int kThreads = kWGThreads + 32 * (1 + kMmaWarps);  // 640
-constexpr int kASlots = 6;                 // tensor-memory A ring
-constexpr int kDSlots = 4;                 // tensor-memory accumulator ring
+constexpr int kStageTiles = 2;             // tiles per bulk copy and stage: 17,408-byte copies keep
+                                           // the copy engine near the HBM rate with few stages
+constexpr int kStageBytes = kStageTiles * kTileBytes;
+constexpr int kStages = 5;
+constexpr int kConvWG = 2;                 // converter warpgroups: warps 0-7 (tile i: WG i % 2)
+constexpr int kEpiWG = 3;                  // epilogue warpgroups: warps 8-19 (tile i: WG i % 3)
+constexpr int kStreamThreads = 128 * (kConvWG + kEpiWG);  // 640
+constexpr int kSelThreads = 512;           // threads 0-511 run the selection and the exchange
+constexpr int kProducerWarp = kStreamThreads / 32;     // 20
+constexpr int kMmaWarp = kProducerWarp + 1;            // 21: allocates tensor memory; 21-23 issue MMAs
+constexpr int kMmaWarps = 3;                           // tile i is issued by warp kMmaWarp + i % 3
+constexpr int kThreads = kStreamThreads + 32 * (1 + kMmaWarps);  // 768
+constexpr int kASlots = 4;                 // tensor-memory A ring
+constexpr int kDSlots = 5;                 // tensor-memory accumulator ring
+// mbarriers indexed by tile modulo a multiple of both the ring size and the
+// waiters' rotation, so each waiter waits on every phase of its barriers
+constexpr int kAFullBars = 12;             // afull[i % 12]: waited by issuer i % 3
+constexpr int kDFullBars = 15;             // dfull[i % 15]: waited by epilogue WG i % 3
 constexpr int kChunkTiles = 64;
 constexpr int kLocalK = DS4X_TOPK_MAX;     // 512
 // Keys carried from one chunk to the next: every key at or above the bucket
@@ -81,7 +96,7 @@ constexpr int kTopM = 16;                  // fewest candidates a CTA publishes
 constexpr int kCandCap = kLocalK + 64;     // candidates a CTA may publish (its top M and their bucket)
 constexpr int kPubCap = 1024;              // pool slots per CTA; keys a flagged CTA may publish
 constexpr int kPoolPer = 8;                // pool keys each selection thread holds in registers
-constexpr int kPoolCap = kPoolPer * kWGThreads;  // 4096: larger pools take the exact fallback
+constexpr int kPoolCap = kPoolPer * kSelThreads;  // 4096: larger pools take the exact fallback
 constexpr int kRadixBuckets = 2048;        // counting-sort buckets over the kept pool keys
 constexpr int kRankStep = 8;              // candidates ranked together (lane j stores candidate j's partial)
 constexpr int kDirect = 16;                // up to this many candidates a CTA ranks by direct counts
@@ -103,23 +118,24 @@ constexpr uint32_t kLbo = 128;             // next 16-element K chunk
 constexpr uint32_t kSbo = 8 * 128;         // next 8 rows
 constexpr uint32_t kIdesc = idesc_mxf8f6f4_e2m1_e4m3(kN);
 constexpr unsigned long long kTimeoutNs = 500ull * 1000 * 1000;  // a bounded wait gives up after 0.5 s
-constexpr uint32_t kWaitHintNs = 2000;     // a waiting thread may sleep in hardware up to 2 us per poll
-constexpr uint32_t kBarSel = 1;            // named barrier of the 512 warpgroup threads
-constexpr uint32_t kBarEpi0 = 2;           // epilogue warpgroup e: named barrier kBarEpi0 + e (128 threads)
+constexpr uint32_t kBarSel = 1;            // named barrier of the 512 selection threads
+constexpr uint32_t kBarStream = 2;         // named barrier of the 640 converter and epilogue threads
 // An mbarrier parity wait for phase c passes early if phase c - 1 is still
 // open, so each parity wait below is done by a thread (or warpgroup) that also
 // waited for the slot's previous phase: the slot counts are multiples of the
 // waiters' rotation.  The MMA warps' wait for a free accumulator slot (three
-// issuers, four slots) uses a monotonic counter instead (dfree).
-static_assert(kStages % kConvWG == 0, "a stage's phases are waited on by one converter warpgroup");
-static_assert(kASlots % kMmaWarps == 0 && kASlots % kConvWG == 0, "an A slot's phases: one issuer, one converter WG");
-static_assert(kDSlots % kEpiWG == 0, "an accumulator slot's full phases: one epilogue warpgroup");
+// issuers, four slots) uses a monotonic counter instead (drel: each epilogue
+// warp adds one with release semantics once it has read its lanes).
+static_assert(kStageTiles == kConvWG, "each converter warpgroup takes one tile of every stage");
+static_assert(kASlots % kConvWG == 0, "an A slot's empty phases: one converter WG");
+static_assert(kAFullBars % kASlots == 0 && kAFullBars % kMmaWarps == 0, "afull: one issuer per barrier");
+static_assert(kDFullBars % kDSlots == 0 && kDFullBars % kEpiWG == 0, "dfull: one epilogue WG per barrier");
 static_assert(kDSlots * 64 <= int(kACol0) && kACol0 + 32 * kASlots <= kSfaCol0 && kSfbLoCol + 4 <= uint32_t(kTmemCols),
               "tensor-memory map");
 static_assert(kSfaCol0 % 4 == 0 && kSfbCol % 4 == 0 && kSfbLoCol % 4 == 0,
               "scale-factor columns start on a 4-column boundary");
-static_assert(kSelPerThread * kWGThreads >= kKeysCap, "selection registers cover the key buffer");
-static_assert(kKeysCap * 8 <= kStages * kTileBytes, "the key buffer fits the stage ring (the exact top-M copy)");
+static_assert(kSelPerThread * kSelThreads >= kKeysCap, "selection registers cover the key buffer");
+static_assert(kKeysCap * 8 <= kStages * kStageBytes, "the key buffer fits the stage ring (the exact top-M copy)");
 constexpr int kMaxDynSmem = 232448;         // 227 KB per CTA on sm_103
 
 // Byte offset of (row r, K element kk) in a canonical no-swizzle K-major
@@ -142,7 +158,7 @@ struct SelShared {
 
 struct __align__(1024) Smem {
   uint8_t bq[kOpBytes];                       // query pieces, E4M3, canonical K-major (B)
-  uint8_t stage[kStages][kTileBytes];         // raw tile ring
+  uint8_t stage[kStages][kStageBytes];        // raw tile ring, two tiles a stage
   unsigned long long keys[kKeysCap];          // [0, 1024): carried keys; then the chunk's keys
   unsigned long long out[kLocalK];
   unsigned long long sortbuf[2 * kLocalK];
@@ -150,8 +166,8 @@ struct __align__(1024) Smem {
   alignas(16) float wq[DS4X_IDX_HEADS];       // head weights
   uint8_t sfb[2 * DS4X_IDX_HEADS][4];         // query-piece scale bytes per 32-element block (hi rows, lo rows)
   unsigned long long full[kStages], empty[kStages];
-  unsigned long long afull[kASlots], aempty[kASlots], dfull[kDSlots];
-  int dfree[kDSlots];                         // last tile whose epilogue released the slot (-1: none)
+  unsigned long long afull[kAFullBars], aempty[kASlots], dfull[kDFullBars];
+  int drel[kDSlots];                          // warps of the epilogue that released the slot so far
   unsigned long long epoch_full;               // the producer has stored `epoch`
   SelShared sel;
   unsigned long long cand[kCandCap];          // this CTA's candidates
@@ -193,7 +209,7 @@ __device__ bool wait_bar(Smem &sm, unsigned long long *bar, uint32_t parity, WsH
   if (mbar_try_wait(b, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait_sleep(b, parity, kWaitHintNs)) return true;
+    if (mbar_try_wait(b, parity)) return true;
     if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) return false;
     if (globaltimer() - t0 > kTimeoutNs) {
       atomicExch(&hdr->status, int32_t(DS4X_ETIMEOUT));
@@ -211,8 +227,8 @@ __device__ __forceinline__ void fma_f32x2(float &a0, float &a1, float w0, float 
       : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
-__device__ __forceinline__ void st_release_shared(int *p, int v) {
-  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_add_shared(int *p, int v) {
+  asm volatile("red.release.cta.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ int ld_acquire_shared(const int *p) {
   int v;
@@ -265,7 +281,9 @@ __device__ __forceinline__ void hist_add(uint32_t *hist, int b) {
   atomicAdd(&hist[b >> 1], 1u << ((b & 1) * 16));
 }
 
-__device__ __forceinline__ void bar512() { named_bar_sync(kBarSel, kWGThreads); }
+__device__ __forceinline__ void bar512() { named_bar_sync(kBarSel, kSelThreads); }
+// all converter and epilogue threads (the chunk ends)
+__device__ __forceinline__ void bar_stream() { named_bar_sync(kBarStream, kStreamThreads); }
 
 // Warp-aggregated append: every lane of the warp calls it; lanes with pred
 // get consecutive slots from *counter (one shared atomic per warp instead of
@@ -305,13 +323,13 @@ __device__ unsigned long long warp_sort32_desc(unsigned long long v, int lane) {
 // double-buffered shared array, one barrier per such stage).
 __device__ unsigned long long block_sort512_desc(unsigned long long v, unsigned long long *buf, int tid) {
   int pb = 0;
-  for (int size = 2; size <= kWGThreads; size <<= 1) {
+  for (int size = 2; size <= kSelThreads; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       unsigned long long o;
       if (stride >= 32) {
-        buf[pb * kWGThreads + tid] = v;
+        buf[pb * kSelThreads + tid] = v;
         bar512();
-        o = buf[pb * kWGThreads + (tid ^ stride)];
+        o = buf[pb * kSelThreads + (tid ^ stride)];
         pb ^= 1;
       } else {
         o = __shfl_xor_sync(0xffffffffu, v, stride);
@@ -346,7 +364,7 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
     int lcnt = 0;
 #pragma unroll
     for (int q = 0; q < kSelPerThread; ++q) {
-      const int i = tid + q * kWGThreads;
+      const int i = tid + q * kSelThreads;
       v[q] = i < cur_n ? list[i] : 0ull;
       if (v[q] != 0) {
         lmin = min(lmin, v[q]);
@@ -364,11 +382,11 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
       sh.red_max[warp] = lmax;
       sh.red_cnt[warp] = lcnt;
     }
-    for (int b = tid; b < kAdaptBuckets; b += kWGThreads) hist[b] = 0;
+    for (int b = tid; b < kAdaptBuckets; b += kSelThreads) hist[b] = 0;
     bar512();
     unsigned long long kmin = ~0ull, kmax = 0;
     int nz = 0;
-    for (int w = 0; w < kWGThreads / 32; ++w) {
+    for (int w = 0; w < kSelThreads / 32; ++w) {
       kmin = min(kmin, sh.red_min[w]);
       kmax = max(kmax, sh.red_max[w]);
       nz += sh.red_cnt[w];
@@ -431,7 +449,7 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
     cur_n = bcnt;
     const int base = sh.out_cnt;
     if (bcnt == need) {
-      for (int i = tid; i < bcnt; i += kWGThreads) out[base + i] = list[i];
+      for (int i = tid; i < bcnt; i += kSelThreads) out[base + i] = list[i];
       bar512();
       if (tid == 0) sh.out_cnt += bcnt;
       bar512();
@@ -447,7 +465,7 @@ __device__ int select_top(unsigned long long *list, int n, int K, unsigned long 
       bar512();
       break;
     }
-    if (bcnt <= kWGThreads) {
+    if (bcnt <= kSelThreads) {
       const unsigned long long s = block_sort512_desc(tid < bcnt ? list[tid] : 0ull, sortbuf, tid);
       if (tid < need) out[base + tid] = s;
       bar512();
@@ -472,12 +490,12 @@ __device__ void bucket_rank(const unsigned long long *pool, int n, const unsigne
                             unsigned long long *sorted, SelShared &sh, int tid, int32_t *out_idx,
                             float *out_score) {
   constexpr int kB = kRadixBuckets;
-  static_assert(kB == 4 * kWGThreads, "four buckets per thread");
+  static_assert(kB == 4 * kSelThreads, "four buckets per thread");
   const int lane = tid & 31, warp = tid >> 5;
   const unsigned long long range = hi - lo;
   const int shift = range < kB ? 0 : (64 - __clzll((long long)range)) - 11;  // range >> shift < 2048
   auto bucket = [&](unsigned long long x) { return kB - 1 - int((x - lo) >> shift); };
-  for (int i = tid; i < n; i += kWGThreads) atomicAdd(&hist[bucket(pool[i])], 1u);
+  for (int i = tid; i < n; i += kSelThreads) atomicAdd(&hist[bucket(pool[i])], 1u);
   bar512();
   {  // exclusive scan in place: hist[b] = keys in the buckets above b (thread t: buckets 4t .. 4t + 3)
     const uint4 c4 = reinterpret_cast<const uint4 *>(hist)[tid];
@@ -501,13 +519,13 @@ __device__ void bucket_rank(const unsigned long long *pool, int n, const unsigne
     reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(a0, a1, a2, a3);
   }
   bar512();
-  for (int i = tid; i < n; i += kWGThreads) {  // counting-sort scatter: bucket by bucket, from the top
+  for (int i = tid; i < n; i += kSelThreads) {  // counting-sort scatter: bucket by bucket, from the top
     const unsigned long long x = pool[i];
     sorted[atomicAdd(&hist[bucket(x)], 1u)] = x;
   }
   bar512();
   // hist[b] is now the end of bucket b, the start of bucket b + 1
-  for (int e = tid; e < nc; e += kWGThreads) {
+  for (int e = tid; e < nc; e += kSelThreads) {
     const unsigned long long x = cand[e];
     const int b = bucket(x);
     const int s0 = b == 0 ? 0 : int(hist[b - 1]), s1 = int(hist[b]);
@@ -672,11 +690,13 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   const int n_tiles = int(tile_end - tile_begin);
   WsHeader *hdr = &ws->hdr;
 
-  // tile i of this CTA -> stage i % kStages (producer thread)
-  auto issue_tile = [&](int i) {
-    const int s = i % kStages;
-    const int64_t r0 = (tile_begin + i) * kTileRows;
-    const int nr = n_rows - r0 < kTileRows ? int(n_rows - r0) : kTileRows;
+  // tiles 2j and 2j + 1 of this CTA -> stage j % kStages, one bulk copy (producer thread)
+  const int n_stage_copies = (n_tiles + kStageTiles - 1) / kStageTiles;
+  auto issue_stage = [&](int j) {
+    const int s = j % kStages;
+    const int64_t r0 = (tile_begin + int64_t(kStageTiles) * j) * kTileRows;
+    const int64_t left = n_rows - r0;
+    const int nr = left < kStageTiles * kTileRows ? int(left) : kStageTiles * kTileRows;
     const uint32_t bytes = uint32_t(nr) * DS4X_IDX_ROW_BYTES;
     const uint32_t bulk = bytes & ~15u;
     const uint8_t *src = rows + r0 * DS4X_IDX_ROW_BYTES;
@@ -690,28 +710,24 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
   if (tid == kProducerWarp * 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kTileRows);
+      mbar_init(smem_u32(&sm.empty[s]), kStageTiles * kTileRows);  // each converter thread, once per stage
     }
-    for (int j = 0; j < kASlots; ++j) {
-      mbar_init(smem_u32(&sm.afull[j]), kTileRows);
-      mbar_init(smem_u32(&sm.aempty[j]), 1);
-    }
-    for (int j = 0; j < kDSlots; ++j) {
-      mbar_init(smem_u32(&sm.dfull[j]), 1);
-      sm.dfree[j] = -1;
-    }
+    for (int j = 0; j < kAFullBars; ++j) mbar_init(smem_u32(&sm.afull[j]), kTileRows);
+    for (int j = 0; j < kASlots; ++j) mbar_init(smem_u32(&sm.aempty[j]), 1);
+    for (int j = 0; j < kDFullBars; ++j) mbar_init(smem_u32(&sm.dfull[j]), 1);
+    for (int j = 0; j < kDSlots; ++j) sm.drel[j] = 0;
     mbar_init(smem_u32(&sm.epoch_full), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    // the first tiles go out now, under the set-up below
-    for (int i = 0; i < kStages && i < n_tiles; ++i) issue_tile(i);
+    // the first stages go out now, under the set-up below
+    for (int j = 0; j < kStages && j < n_stage_copies; ++j) issue_stage(j);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
   }
   bool lo_nonzero = false;
-  if (tid < kWGThreads) {
+  if (tid < kSelThreads) {
     // query -> two E4M3 pieces per 32-element block (B rows h and 64 + h);
     // thread t < 256 takes head t / 4, block t % 4 (32 elements, 64 bytes)
     if (tid < DS4X_IDX_HEADS * 4) {
@@ -754,7 +770,16 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
         const uint32_t c2 = cvt_e4m3x2(x[2 * j + 1] * s_lo, x[2 * j] * s_lo);
         if (j & 1) lw[j >> 1] |= c2 << 16; else lw[j >> 1] = c2;
       }
-      // elements 32 b .. 32 b + 31 are two 16-element chunks of rows h and 64 + h
+      // elements 32 b .. 32 b + 31 are two 16-element chunks of rows h and 64 + h,
+      // each group of eight in the converter's K order (even elements, then odd)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t a = hw[2 * g], c = hw[2 * g + 1], la = lw[2 * g], lc = lw[2 * g + 1];
+        hw[2 * g] = __byte_perm(a, c, 0x6420);
+        hw[2 * g + 1] = __byte_perm(a, c, 0x7531);
+        lw[2 * g] = __byte_perm(la, lc, 0x6420);
+        lw[2 * g + 1] = __byte_perm(la, lc, 0x7531);
+      }
       *reinterpret_cast<uint4 *>(sm.bq + op_offset(h, 32 * b)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4 *>(sm.bq + op_offset(h, 32 * b + 16)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
       *reinterpret_cast<uint4 *>(sm.bq + op_offset(DS4X_IDX_HEADS + h, 32 * b)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -765,9 +790,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) lo_nonzero |= (lw[j] & 0x7f7f7f7fu) != 0u;  // any nonzero lo code (0x80 is -0)
     }
-    for (int h = tid; h < DS4X_IDX_HEADS; h += kWGThreads) sm.wq[h] = w[h];
-    for (int i = tid; i < kKeysCap; i += kWGThreads) sm.keys[i] = 0ull;
-    for (int i = tid; i < kHistWords; i += kWGThreads) sm.hist[i] = 0u;
+    for (int h = tid; h < DS4X_IDX_HEADS; h += kSelThreads) sm.wq[h] = w[h];
+    for (int i = tid; i < kKeysCap; i += kSelThreads) sm.keys[i] = 0ull;
+    for (int i = tid; i < kHistWords; i += kSelThreads) sm.hist[i] = 0u;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -798,16 +823,16 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       // stored once the copies are out
       uint32_t epoch;
       asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(epoch) : "l"(&ws->sync[sess].epoch) : "memory");
-      int issued = min(kStages, n_tiles);  // issued during the set-up
-      for (int i = issued; i < n_tiles; ++i) {
-        if (!wait_bar(sm, &sm.empty[i % kStages], ((i / kStages) - 1) & 1, hdr)) break;
-        issue_tile(i);
-        issued = i + 1;
+      int issued = min(kStages, n_stage_copies);  // issued during the set-up
+      for (int j = issued; j < n_stage_copies; ++j) {
+        if (!wait_bar(sm, &sm.empty[j % kStages], ((j / kStages) - 1) & 1, hdr)) break;
+        issue_stage(j);
+        issued = j + 1;
       }
       sm.epoch = epoch;
       mbar_arrive(smem_u32(&sm.epoch_full));
       if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
-        for (int i = max(0, issued - kStages); i < issued; ++i) drain_bar(&sm.full[i % kStages], (i / kStages) & 1);
+        for (int j = max(0, issued - kStages); j < issued; ++j) drain_bar(&sm.full[j % kStages], (j / kStages) & 1);
       }
     }
   } else if (warp >= kMmaWarp) {
@@ -818,8 +843,9 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       int issued = 0;
       for (int i = warp - kMmaWarp; i < n_tiles; i += kMmaWarps) {
         const int a = i % kASlots, d = i % kDSlots;
-        if (!wait_bar(sm, &sm.afull[a], (i / kASlots) & 1, hdr)) break;
-        if (i >= kDSlots && !wait_seq(sm, &sm.dfree[d], i - kDSlots, hdr)) break;
+        if (!wait_bar(sm, &sm.afull[i % kAFullBars], (i / kAFullBars) & 1, hdr)) break;
+        // slot d's earlier uses (tiles i - kDSlots, i - 2 kDSlots, ...) each end with four releases
+        if (i >= kDSlots && !wait_seq(sm, &sm.drel[d], 4 * (i / kDSlots), hdr)) break;
         tc_fence_after();
         if (lo_any)
           mma_mxf8f6f4_ta_k128_2b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a),
@@ -829,12 +855,12 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           mma_mxf8f6f4_ta_k128_1b(tmem_base + kDCol0 + uint32_t(64 * d), tmem_base + kACol0 + uint32_t(32 * a),
                                   bdesc_hi, kIdesc, tmem_base + kSfaCol0 + uint32_t(4 * a), tmem_base + kSfbCol);
         tc_commit(smem_u32(&sm.aempty[a]));
-        tc_commit(smem_u32(&sm.dfull[d]));
+        tc_commit(smem_u32(&sm.dfull[i % kDFullBars]));
         issued = i + 1;
       }
       if (*reinterpret_cast<volatile int *>(&sm.abort_flag) && issued > 0) {
         const int i = issued - 1;  // this thread's last commit covers all of its MMAs
-        drain_bar(&sm.dfull[i % kDSlots], (i / kDSlots) & 1);
+        drain_bar(&sm.dfull[i % kDFullBars], (i / kDFullBars) & 1);
       }
     }
   } else if (warp < kProducerWarp) {
@@ -849,34 +875,38 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
       for (int i = c0 + role_wg; i < c1; i += n_role_wg) {
         if (is_conv) {
           // ---- raw row -> A slot (one code per byte) + scale-factor word -----
-          const int st = i % kStages, a = i % kASlots;
-          wait_bar(sm, &sm.full[st], (i / kStages) & 1, hdr);
+          const int j = i / kStageTiles, st = j % kStages, a = i % kASlots;
+          wait_bar(sm, &sm.full[st], (j / kStages) & 1, hdr);
           uint32_t wd[17];
-          const uint32_t *rp = reinterpret_cast<const uint32_t *>(sm.stage[st] + r * DS4X_IDX_ROW_BYTES);
+          const uint32_t *rp = reinterpret_cast<const uint32_t *>(sm.stage[st] + (i % kStageTiles) * kTileBytes +
+                                                                   r * DS4X_IDX_ROW_BYTES);
 #pragma unroll
           for (int t = 0; t < 17; ++t) wd[t] = rp[t];
           mbar_arrive(smem_u32(&sm.empty[st]));
           if (i >= kASlots) wait_bar(sm, &sm.aempty[a], ((i / kASlots) - 1) & 1, hdr);
-          // word t holds codes 8t..8t+7 (even code in the low nibble); column c
-          // of the slot takes codes 4c..4c+3, one per byte, shifted to bits 5-2
+          // word t holds codes 8t..8t+7 (even code in the low nibble).  Each
+          // code goes to its own byte, in bits 5-2 with bits 1-0 clear (the
+          // container reads bits 5-0; bits 7-6 are ignored); column 2t takes the
+          // even codes 8t, 8t+2, 8t+4, 8t+6 and column 2t+1 the odd ones, so K
+          // runs in that order within each group of eight (the query pieces
+          // are stored in the same order; a block's 32 codes stay in its four
+          // columns, so the block scales are untouched)
           uint32_t av[32];
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            const uint32_t ev = (wd[t] << 2) & 0x3c3c3c3cu;  // codes 8t, 8t+2, 8t+4, 8t+6
-            const uint32_t od = (wd[t] >> 2) & 0x3c3c3c3cu;  // codes 8t+1, 8t+3, 8t+5, 8t+7
-            av[2 * t] = __byte_perm(ev, od, 0x5140);
-            av[2 * t + 1] = __byte_perm(ev, od, 0x7362);
+            av[2 * t] = (wd[t] & 0x0f0f0f0fu) << 2;
+            av[2 * t + 1] = (wd[t] & 0xf0f0f0f0u) >> 2;
           }
           tc_st_x32(tmem_base + lane_base + kACol0 + uint32_t(32 * a), av);
           // row r's scales: lane r, column kSfaCol0 + 4 a + r / 32
           tc_st_x1(tmem_base + lane_base + kSfaCol0 + uint32_t(4 * a + (warp & 3)), wd[16]);
           tc_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&sm.afull[a]));
+          mbar_arrive(smem_u32(&sm.afull[i % kAFullBars]));
         } else {
           // ---- epilogue: accumulators -> score -> key --------------------------
           const int d = i % kDSlots;
-          const bool ok = wait_bar(sm, &sm.dfull[d], (i / kDSlots) & 1, hdr);
+          const bool ok = wait_bar(sm, &sm.dfull[i % kDFullBars], (i / kDFullBars) & 1, hdr);
           tc_fence_after();
           const uint32_t d_t = tmem_base + lane_base + kDCol0 + uint32_t(64 * d);
           const float4 *w4 = reinterpret_cast<const float4 *>(sm.wq);
@@ -888,10 +918,10 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
             tc_ld_x16(d_t + uint32_t(32 * half + 16), v1);
             tc_wait_ld();
             if (half == 1) {
-              // the warpgroup has read the slot: its first thread publishes the tile
+              // this warp has read its 32 lanes of the slot: count one release
               tc_fence_before();
-              named_bar_sync(kBarEpi0 + uint32_t(role_wg), 128);
-              if (r == 0) st_release_shared(&sm.dfree[d], i);
+              __syncwarp();
+              if (lane == 0) red_release_add_shared(&sm.drel[d], 1);
             }
 #pragma unroll
             for (int g = 0; g < 8; ++g) {  // heads 32 half + 4 g .. + 3
@@ -913,7 +943,7 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
           sm.keys[kCarry + (i - c0) * kTileRows + r] = key;
         }
       }
-      bar512();
+      bar_stream();
 
       // ---- end of chunk ---------------------------------------------------------
       const int n_in = kCarry + (c1 - c0) * kTileRows;
@@ -921,356 +951,361 @@ score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
         last_n_in = n_in;
         break;
       }
-      // keep a superset of the local top-512 for the next chunk
-      hist_cuts(sm.hist, sm.sel, tid, kTopM);
-      const int b512 = sm.sel.c512_b;  // -1: at most 512 keys, keep all
-      unsigned long long v[kSelPerThread];
-#pragma unroll
-      for (int qq = 0; qq < kSelPerThread; ++qq) {
-        const int i = tid + qq * kWGThreads;
-        v[qq] = i < n_in ? sm.keys[i] : 0ull;
-      }
-      if (tid == 0) sm.sel.list_cnt = 0;
-      bar512();
-      {
-        // one shared atomic per warp for the whole pass
-        unsigned masks[kSelPerThread];
-        int total = 0;
-#pragma unroll
+      if (tid < kSelThreads) {  // threads 512-639 (the third epilogue warpgroup) wait below
+        // keep a superset of the local top-512 for the next chunk
+        hist_cuts(sm.hist, sm.sel, tid, kTopM);
+        const int b512 = sm.sel.c512_b;  // -1: at most 512 keys, keep all
+        unsigned long long v[kSelPerThread];
+  #pragma unroll
         for (int qq = 0; qq < kSelPerThread; ++qq) {
-          const int b = v[qq] != 0ull ? fixed_bucket(v[qq]) : -2;
-          masks[qq] = __ballot_sync(0xffffffffu, b >= b512 && b >= 0);
-          total += __popc(masks[qq]);
+          const int i = tid + qq * kSelThreads;
+          v[qq] = i < n_in ? sm.keys[i] : 0ull;
         }
-        int base = 0;
-        if (lane == 0 && total > 0) base = atomicAdd(&sm.sel.list_cnt, total);
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-        for (int qq = 0; qq < kSelPerThread; ++qq) {
-          if (masks[qq] & (1u << lane)) sm.keys[base + __popc(masks[qq] & lt)] = v[qq];
-          base += __popc(masks[qq]);
-        }
-      }
-      bar512();
-      int n_keep = sm.sel.list_cnt;
-      // the rest of the carried region is zero (the chunk region is rewritten whole)
-      for (int i = n_keep + tid; i < kCarry; i += kWGThreads) sm.keys[i] = 0ull;
-      bar512();
-      if (n_keep > kCarry) {  // a very wide boundary bucket: reduce exactly to 512
-        const int m = select_top(sm.keys, n_keep, kLocalK, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-        for (int i = tid; i < kCarry; i += kWGThreads) sm.keys[i] = i < m ? sm.out[i] : 0ull;
+        if (tid == 0) sm.sel.list_cnt = 0;
         bar512();
-        n_keep = m;
-      }
-      // histogram of the carried keys for the next chunk
-      for (int i = tid; i < kHistWords; i += kWGThreads) sm.hist[i] = 0u;
-      bar512();
-      for (int i = tid; i < n_keep; i += kWGThreads) hist_add(sm.hist, fixed_bucket(sm.keys[i]));
-      bar512();
-    }
-
-    // The next kernel in the stream (the attention, launched as a programmatic
-    // dependent) may take an SM as soon as this grid's CTAs leave; it waits
-    // for the whole grid before it reads the indices.
-    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    // ---- this CTA's candidates ------------------------------------------------
-    // The CTA publishes its keys down to the bucket of its M-th key (all of
-    // them when it has few) with a bound th that every key it leaves out is
-    // below.  M covers about k / Gs winners per CTA with a wide margin; any M
-    // gives the exact result, a small one only makes the fallback likelier.
-    if (tid == 0) sm.sel.ok = wait_bar(sm, &sm.epoch_full, 0, hdr) && !*reinterpret_cast<volatile int *>(&sm.abort_flag);
-    const int n_in = last_n_in;
-    const float lam = float(k) / float(Gs);
-    const int M = min(k, max(kTopM, int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f))));
-    hist_cuts(sm.hist, sm.sel, tid, M);
-    if (sm.sel.ok) {
-      const int total = sm.sel.total, bM = sm.sel.cM_b;
-      // 0: every key; 1: the keys in buckets >= bM; 2: more than kCandCap of those, the exact top M
-      const int mode =
-          total <= M + 32 ? 0 : (sm.sel.cM_above + sm.sel.cM_cnt <= kCandCap ? 1 : 2);
-      const int ncand = mode == 0 ? total : (mode == 1 ? sm.sel.cM_above + sm.sel.cM_cnt : M);
-      SessSync &ss = ws->sync[sess];
-      const uint32_t par = sm.epoch & 1u;
-      unsigned long long reserved = 0ull;
-      if (tid == 0 && Gs > 1) reserved = atomicAdd(&ss.main[par], static_cast<unsigned long long>(ncand));
-      if (mode != 2) {
-        // every key at or above the bucket's floor (mode 0: every key); few
-        // qualify, so a warp appends only when one of its lanes has one
-        const unsigned long long thr =
-            (mode == 0 || bM == 0) ? 1ull : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
-        const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(sm.keys);
-        for (int j = tid; 2 * j < n_in; j += kWGThreads) {
-          const ulonglong2 kv = k2[j];  // n_in is even
-          const bool c0 = kv.x >= thr, c1 = kv.y >= thr;
-          if (__any_sync(__activemask(), c0 || c1)) {
-            const unsigned act = __activemask();
-            const unsigned m0 = __ballot_sync(act, c0), m1 = __ballot_sync(act, c1);
-            const int leader = __ffs(act) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&sm.sel.fill, __popc(m0) + __popc(m1));
-            base = __shfl_sync(act, base, leader);
-            const unsigned lt = (1u << lane) - 1u;
-            const int p0 = base + __popc(m0 & lt), p1 = base + __popc(m0) + __popc(m1 & lt);
-            if (c0 && p0 < kCandCap) sm.cand[p0] = kv.x;
-            if (c1 && p1 < kCandCap) sm.cand[p1] = kv.y;
-          }
-        }
-        // the bucket's floor (bucket 0 also holds everything below it: nothing is left out)
-        if (tid == 0)
-          sm.th = (mode == 0 || bM == 0) ? 0ull
-                                         : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
-      } else {
-        unsigned long long *scratch = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
-        for (int i = tid; i < n_in; i += kWGThreads) scratch[i] = sm.keys[i];
-        bar512();
-        select_top(scratch, n_in, M, sm.cand, sm.hist, sm.sortbuf, sm.sel, tid);
-        if (warp == 0) {
-          unsigned long long t = ~0ull;
-          for (int i = lane; i < M; i += 32) t = min(t, sm.cand[i]);
-          for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
-          if (lane == 0) sm.th = t;
-        }
-      }
-      if (tid == 0) sm.sel.base = uint32_t(reserved);
-      bar512();
-
-      // ---- exchange: publish, meet, load the session's candidates ------------------
-      const unsigned long long th = sm.th;
-      unsigned long long *pool_g = ws->pool + size_t(cta0) * kPubCap;
-      if (Gs > 1) {
-        const uint32_t base = sm.sel.base;
-        for (int i = tid; i < ncand; i += kWGThreads) pool_g[base + i] = sm.cand[i];
-        if (tid == 0) atomicMax(&ss.thm[par], th);
-      }
-      reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the counting sort's 2048 buckets
-      if (tid == 0) {
-        sm.sel.ncol = 0;
-        sm.sel.nhi = 0;
-        sm.sel.nge = 0;
-        sm.sel.wcnt = 0;
-        sm.sel.pub_cnt = 0;
-      }
-      bar512();
-      int n_all = ncand;
-      unsigned long long thmax = th;
-      if (Gs > 1) {
-        if (tid == 0) {
-          if (int(blockIdx.x) == cta0) {  // the next exchange's words: nothing in this launch uses them
-            ss.main[par ^ 1u] = 0ull;
-            ss.fb[par ^ 1u] = 0ull;
-            ss.thm[par ^ 1u] = 0ull;
-          }
-          red_release_add(&ss.main[par], 1ull << 32);
-          unsigned long long seen = 0ull;
-          const unsigned extra = __ldcg(&hdr->wait_extra);
-          const bool ok = wait_arrivals(&ss.main[par], unsigned(Gs) + extra, hdr, &seen);
-          if (ok && int(blockIdx.x) == cta0) ss.epoch = sm.epoch + 1u;
-          sm.sel.n_all = int(uint32_t(seen));
-          sm.sel.ok = ok ? 1 : 0;
-        }
-        bar512();
-        n_all = sm.sel.n_all;
-        thmax = ld_cg(&ss.thm[par]);
-      }
-      const bool overflow = n_all > kPoolCap;
-      if (sm.sel.ok) {
-        // The pool keys at or above the largest bound, compacted into pool_s
-        // (the stage ring is free now): no key below it can be above a
-        // winner, and when none of the CTAs is flagged the winners are among
-        // them.  Their count decides whether any CTA is flagged.
-        unsigned long long *pool_s = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
-        static_assert(kPoolCap * 8 <= kStages * kTileBytes, "the pool fits in the stage ring");
         {
-          unsigned long long v[kPoolPer];
-#pragma unroll
-          for (int q = 0; q < kPoolPer; ++q) {
-            const int i = tid + q * kWGThreads;
-            v[q] = (!overflow && i < n_all) ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
-          }
-          unsigned keep = 0u, mn = ~0u, mx = 0u;
-          int cnt = 0;
-#pragma unroll
-          for (int q = 0; q < kPoolPer; ++q) {
-            const bool kq = v[q] != 0ull && v[q] >= thmax;
-            keep |= kq ? (1u << q) : 0u;
-            cnt += __popc(__ballot_sync(0xffffffffu, kq));
-            if (kq) {
-              const uint32_t h = uint32_t(v[q] >> 32);
-              mn = min(mn, h);
-              mx = max(mx, h);
-            }
+          // one shared atomic per warp for the whole pass
+          unsigned masks[kSelPerThread];
+          int total = 0;
+  #pragma unroll
+          for (int qq = 0; qq < kSelPerThread; ++qq) {
+            const int b = v[qq] != 0ull ? fixed_bucket(v[qq]) : -2;
+            masks[qq] = __ballot_sync(0xffffffffu, b >= b512 && b >= 0);
+            total += __popc(masks[qq]);
           }
           int base = 0;
-          if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.nge, cnt);
+          if (lane == 0 && total > 0) base = atomicAdd(&sm.sel.list_cnt, total);
           base = __shfl_sync(0xffffffffu, base, 0);
           const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-          for (int q = 0; q < kPoolPer; ++q) {
-            const bool kq = (keep >> q) & 1u;
-            const unsigned mk = __ballot_sync(0xffffffffu, kq);
-            if (kq) pool_s[base + __popc(mk & lt)] = v[q];
-            base += __popc(mk);
+  #pragma unroll
+          for (int qq = 0; qq < kSelPerThread; ++qq) {
+            if (masks[qq] & (1u << lane)) sm.keys[base + __popc(masks[qq] & lt)] = v[qq];
+            base += __popc(masks[qq]);
           }
-          mn = __reduce_min_sync(0xffffffffu, mn);
-          mx = __reduce_max_sync(0xffffffffu, mx);
-          if (lane == 0) {
-            sm.sel.red_lo[warp] = mn;
-            sm.sel.red_hi[warp] = mx;
-          }
-        }
-        // this CTA's candidates at or above the largest bound, into sortbuf
-        for (int e0 = 0; e0 < ncand; e0 += kWGThreads) {
-          const int e = e0 + tid;
-          const unsigned long long x = e < ncand ? sm.cand[e] : 0ull;
-          const bool h = x != 0ull && x >= thmax;
-          const int p = warp_append(&sm.sel.nhi, h);
-          if (h) sm.sortbuf[p] = x;
         }
         bar512();
-        const int n_ge = sm.sel.nge;
-        // No CTA left out a key above the k-th candidate: the pool holds the
-        // session's top-k.  (One CTA: its candidates always do.)
-        const bool fast = !overflow && (Gs == 1 || (n_all < k ? thmax == 0ull : n_ge >= k));
-        if (fast) {
-          // Every winner is one of some CTA's candidates at or above the
-          // largest bound, and a candidate wins iff fewer than k pool keys
-          // are above it; its rank is that count.
-          const int nhi = sm.sel.nhi;
-          const int nwin = min(n_all, k);
-          if (nhi <= kDirect) {
-            // per-warp partial counts, in the histogram's words (unused on this path)
-            int *rank_part = reinterpret_cast<int *>(sm.hist);
-            static_assert((kWGThreads / 32) * kDirect <= kHistWords, "rank partials fit the histogram words");
-            for (int e0 = 0; e0 < nhi; e0 += kRankStep) {
-              unsigned long long x[kRankStep];
-              unsigned r[kRankStep];
-#pragma unroll
-              for (int j = 0; j < kRankStep; ++j) {
-                x[j] = e0 + j < nhi ? sm.sortbuf[e0 + j] : ~0ull;
-                r[j] = 0u;
-              }
-#pragma unroll
-              for (int q = 0; q < kPoolPer; ++q) {
-                if (q * kWGThreads >= n_ge) break;
-                const int i = q * kWGThreads + tid;
-                const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
-#pragma unroll
-                for (int j = 0; j < kRankStep; ++j) r[j] += pv > x[j] ? 1u : 0u;
-              }
-#pragma unroll
-              for (int j = 0; j < kRankStep; ++j) r[j] = __reduce_add_sync(0xffffffffu, r[j]);
-              unsigned mine = 0u;
-#pragma unroll
-              for (int j = 0; j < kRankStep; ++j) mine = lane == j ? r[j] : mine;
-              if (lane < kRankStep && e0 + lane < nhi) rank_part[warp * kDirect + e0 + lane] = int(mine);
-            }
-            bar512();
-            for (int e = tid; e < nhi; e += kWGThreads) {
-              int r = 0;
-#pragma unroll
-              for (int w = 0; w < kWGThreads / 32; ++w) r += rank_part[w * kDirect + e];
-              if (r < k) {
-                const unsigned long long x = sm.sortbuf[e];
-                out_idx[r] = key_index(x);
-                if (out_score) out_score[r] = key_score(x);
-              }
-            }
-          } else {
-            // more candidates: a counting sort of the kept pool keys ranks them all at once
-            uint32_t mn = ~0u, mx = 0u;
-            for (int w = 0; w < kWGThreads / 32; ++w) {
-              mn = min(mn, sm.sel.red_lo[w]);
-              mx = max(mx, sm.sel.red_hi[w]);
-            }
-            const unsigned long long lo = static_cast<unsigned long long>(mn) << 32;
-            const unsigned long long hi = (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull;
-            static_assert(2 * kPoolCap * 8 <= kStages * kTileBytes, "the pool and its sorted copy fit the stage ring");
-            bucket_rank(pool_s, n_ge, sm.sortbuf, nhi, lo, hi, k, sm.hist, pool_s + kPoolCap, sm.sel, tid, out_idx,
-                        out_score);
-          }
-          if (int(blockIdx.x) == cta0) {
-            for (int e = nwin + tid; e < k; e += kWGThreads) {
-              out_idx[e] = -1;
-              if (out_score) out_score[e] = __uint_as_float(0x7fc00000u);
-            }
-          }
-        } else {
-          // ---- exact fallback -----------------------------------------------------
-          // A CTA whose bound is above the k-th candidate may hold winners it
-          // did not publish: it publishes its local top-k below its bound, and
-          // the session's first CTA merges them with the pool.
-          bool flagged;
-          if (overflow || n_all < k) {
-            flagged = th != 0ull;
-          } else {
-            unsigned c = 0u;
-#pragma unroll
-            for (int q = 0; q < kPoolPer; ++q) {  // the whole pool again (pool_s keeps only the top part)
-              const int i = tid + q * kWGThreads;
-              const unsigned long long pv = i < n_all ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
-              c += (pv != 0ull && pv >= th) ? 1u : 0u;
-            }
-            c = __reduce_add_sync(0xffffffffu, c);
-            bar512();
-            if (lane == 0) sm.sel.red_cnt[warp] = int(c);
-            bar512();
-            int s = 0;
-            for (int w = 0; w < kWGThreads / 32; ++w) s += sm.sel.red_cnt[w];
-            flagged = s < k;
-          }
-          int npub = 0;
-          if (flagged) {
-            const int m = select_top(sm.keys, n_in, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-            for (int i0 = 0; i0 < m; i0 += kWGThreads) {
-              const int i = i0 + tid;
-              const unsigned long long x = i < m ? sm.out[i] : 0ull;
-              const bool pub = x != 0ull && x < th;
-              const int p = warp_append(&sm.sel.pub_cnt, pub);
-              if (pub && p < kPubCap) ws->lists[blockIdx.x][p] = x;
-            }
-            bar512();
-            npub = min(sm.sel.pub_cnt, kPubCap);
-          }
-          if (tid == 0) ws->cnt[blockIdx.x] = npub;
+        int n_keep = sm.sel.list_cnt;
+        // the rest of the carried region is zero (the chunk region is rewritten whole)
+        for (int i = n_keep + tid; i < kCarry; i += kSelThreads) sm.keys[i] = 0ull;
+        bar512();
+        if (n_keep > kCarry) {  // a very wide boundary bucket: reduce exactly to 512
+          const int m = select_top(sm.keys, n_keep, kLocalK, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+          for (int i = tid; i < kCarry; i += kSelThreads) sm.keys[i] = i < m ? sm.out[i] : 0ull;
           bar512();
-          if (tid == 0) red_release_add(&ss.fb[par], 1ull << 32);
-          if (int(blockIdx.x) == cta0) {
-            if (tid == 0) {
-              unsigned long long seen = 0ull;
-              sm.sel.ok = wait_arrivals(&ss.fb[par], unsigned(Gs), hdr, &seen) ? 1 : 0;
-              atomicAdd(&hdr->fallback, 1u);
+          n_keep = m;
+        }
+        // histogram of the carried keys for the next chunk
+        for (int i = tid; i < kHistWords; i += kSelThreads) sm.hist[i] = 0u;
+        bar512();
+        for (int i = tid; i < n_keep; i += kSelThreads) hist_add(sm.hist, fixed_bucket(sm.keys[i]));
+        bar512();
+      }
+      bar_stream();
+    }
+
+    if (tid < kSelThreads) {  // the exchange: threads 0-511
+      // The next kernel in the stream (the attention, launched as a programmatic
+      // dependent) may take an SM as soon as this grid's CTAs leave; it waits
+      // for the whole grid before it reads the indices.
+      if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+      // ---- this CTA's candidates ------------------------------------------------
+      // The CTA publishes its keys down to the bucket of its M-th key (all of
+      // them when it has few) with a bound th that every key it leaves out is
+      // below.  M covers about k / Gs winners per CTA with a wide margin; any M
+      // gives the exact result, a small one only makes the fallback likelier.
+      if (tid == 0) sm.sel.ok = wait_bar(sm, &sm.epoch_full, 0, hdr) && !*reinterpret_cast<volatile int *>(&sm.abort_flag);
+      const int n_in = last_n_in;
+      const float lam = float(k) / float(Gs);
+      const int M = min(k, max(kTopM, int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f))));
+      hist_cuts(sm.hist, sm.sel, tid, M);
+      if (sm.sel.ok) {
+        const int total = sm.sel.total, bM = sm.sel.cM_b;
+        // 0: every key; 1: the keys in buckets >= bM; 2: more than kCandCap of those, the exact top M
+        const int mode =
+            total <= M + 32 ? 0 : (sm.sel.cM_above + sm.sel.cM_cnt <= kCandCap ? 1 : 2);
+        const int ncand = mode == 0 ? total : (mode == 1 ? sm.sel.cM_above + sm.sel.cM_cnt : M);
+        SessSync &ss = ws->sync[sess];
+        const uint32_t par = sm.epoch & 1u;
+        unsigned long long reserved = 0ull;
+        if (tid == 0 && Gs > 1) reserved = atomicAdd(&ss.main[par], static_cast<unsigned long long>(ncand));
+        if (mode != 2) {
+          // every key at or above the bucket's floor (mode 0: every key); few
+          // qualify, so a warp appends only when one of its lanes has one
+          const unsigned long long thr =
+              (mode == 0 || bM == 0) ? 1ull : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
+          const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(sm.keys);
+          for (int j = tid; 2 * j < n_in; j += kSelThreads) {
+            const ulonglong2 kv = k2[j];  // n_in is even
+            const bool c0 = kv.x >= thr, c1 = kv.y >= thr;
+            if (__any_sync(__activemask(), c0 || c1)) {
+              const unsigned act = __activemask();
+              const unsigned m0 = __ballot_sync(act, c0), m1 = __ballot_sync(act, c1);
+              const int leader = __ffs(act) - 1;
+              int base = 0;
+              if (lane == leader) base = atomicAdd(&sm.sel.fill, __popc(m0) + __popc(m1));
+              base = __shfl_sync(act, base, leader);
+              const unsigned lt = (1u << lane) - 1u;
+              const int p0 = base + __popc(m0 & lt), p1 = base + __popc(m0) + __popc(m1 & lt);
+              if (c0 && p0 < kCandCap) sm.cand[p0] = kv.x;
+              if (c1 && p1 < kCandCap) sm.cand[p1] = kv.y;
             }
-            bar512();
-            if (sm.sel.ok) {
-              // the pool and every flagged CTA's list, reduced to the exact top-k
-              int fill = 0;
-              for (int src_i = -1; src_i < Gs; ++src_i) {
-                const unsigned long long *src = src_i < 0 ? pool_g : ws->lists[cta0 + src_i];
-                const int len = src_i < 0 ? (Gs > 1 ? n_all : 0) : min(__ldcg(&ws->cnt[cta0 + src_i]), kPubCap);
-                for (int off = 0; off < len; off += kPubCap) {
-                  const int cl = min(kPubCap, len - off);
-                  if (fill + cl > kKeysCap) {
-                    const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-                    for (int i = tid; i < m; i += kWGThreads) sm.keys[i] = sm.out[i];
-                    bar512();
-                    fill = m;
-                  }
-                  for (int i = tid; i < cl; i += kWGThreads) sm.keys[fill + i] = ld_cg(src + off + i);
-                  fill += cl;
-                  bar512();
+          }
+          // the bucket's floor (bucket 0 also holds everything below it: nothing is left out)
+          if (tid == 0)
+            sm.th = (mode == 0 || bM == 0) ? 0ull
+                                           : static_cast<unsigned long long>(uint32_t(bM + kBuckets) << 18) << 32;
+        } else {
+          unsigned long long *scratch = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
+          for (int i = tid; i < n_in; i += kSelThreads) scratch[i] = sm.keys[i];
+          bar512();
+          select_top(scratch, n_in, M, sm.cand, sm.hist, sm.sortbuf, sm.sel, tid);
+          if (warp == 0) {
+            unsigned long long t = ~0ull;
+            for (int i = lane; i < M; i += 32) t = min(t, sm.cand[i]);
+            for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
+            if (lane == 0) sm.th = t;
+          }
+        }
+        if (tid == 0) sm.sel.base = uint32_t(reserved);
+        bar512();
+
+        // ---- exchange: publish, meet, load the session's candidates ------------------
+        const unsigned long long th = sm.th;
+        unsigned long long *pool_g = ws->pool + size_t(cta0) * kPubCap;
+        if (Gs > 1) {
+          const uint32_t base = sm.sel.base;
+          for (int i = tid; i < ncand; i += kSelThreads) pool_g[base + i] = sm.cand[i];
+          if (tid == 0) atomicMax(&ss.thm[par], th);
+        }
+        reinterpret_cast<uint4 *>(sm.hist)[tid] = make_uint4(0u, 0u, 0u, 0u);  // the counting sort's 2048 buckets
+        if (tid == 0) {
+          sm.sel.ncol = 0;
+          sm.sel.nhi = 0;
+          sm.sel.nge = 0;
+          sm.sel.wcnt = 0;
+          sm.sel.pub_cnt = 0;
+        }
+        bar512();
+        int n_all = ncand;
+        unsigned long long thmax = th;
+        if (Gs > 1) {
+          if (tid == 0) {
+            if (int(blockIdx.x) == cta0) {  // the next exchange's words: nothing in this launch uses them
+              ss.main[par ^ 1u] = 0ull;
+              ss.fb[par ^ 1u] = 0ull;
+              ss.thm[par ^ 1u] = 0ull;
+            }
+            red_release_add(&ss.main[par], 1ull << 32);
+            unsigned long long seen = 0ull;
+            const unsigned extra = __ldcg(&hdr->wait_extra);
+            const bool ok = wait_arrivals(&ss.main[par], unsigned(Gs) + extra, hdr, &seen);
+            if (ok && int(blockIdx.x) == cta0) ss.epoch = sm.epoch + 1u;
+            sm.sel.n_all = int(uint32_t(seen));
+            sm.sel.ok = ok ? 1 : 0;
+          }
+          bar512();
+          n_all = sm.sel.n_all;
+          thmax = ld_cg(&ss.thm[par]);
+        }
+        const bool overflow = n_all > kPoolCap;
+        if (sm.sel.ok) {
+          // The pool keys at or above the largest bound, compacted into pool_s
+          // (the stage ring is free now): no key below it can be above a
+          // winner, and when none of the CTAs is flagged the winners are among
+          // them.  Their count decides whether any CTA is flagged.
+          unsigned long long *pool_s = reinterpret_cast<unsigned long long *>(&sm.stage[0][0]);
+          static_assert(kPoolCap * 8 <= kStages * kStageBytes, "the pool fits in the stage ring");
+          {
+            unsigned long long v[kPoolPer];
+  #pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) {
+              const int i = tid + q * kSelThreads;
+              v[q] = (!overflow && i < n_all) ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
+            }
+            unsigned keep = 0u, mn = ~0u, mx = 0u;
+            int cnt = 0;
+  #pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) {
+              const bool kq = v[q] != 0ull && v[q] >= thmax;
+              keep |= kq ? (1u << q) : 0u;
+              cnt += __popc(__ballot_sync(0xffffffffu, kq));
+              if (kq) {
+                const uint32_t h = uint32_t(v[q] >> 32);
+                mn = min(mn, h);
+                mx = max(mx, h);
+              }
+            }
+            int base = 0;
+            if (lane == 0 && cnt > 0) base = atomicAdd(&sm.sel.nge, cnt);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const unsigned lt = (1u << lane) - 1u;
+  #pragma unroll
+            for (int q = 0; q < kPoolPer; ++q) {
+              const bool kq = (keep >> q) & 1u;
+              const unsigned mk = __ballot_sync(0xffffffffu, kq);
+              if (kq) pool_s[base + __popc(mk & lt)] = v[q];
+              base += __popc(mk);
+            }
+            mn = __reduce_min_sync(0xffffffffu, mn);
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0) {
+              sm.sel.red_lo[warp] = mn;
+              sm.sel.red_hi[warp] = mx;
+            }
+          }
+          // this CTA's candidates at or above the largest bound, into sortbuf
+          for (int e0 = 0; e0 < ncand; e0 += kSelThreads) {
+            const int e = e0 + tid;
+            const unsigned long long x = e < ncand ? sm.cand[e] : 0ull;
+            const bool h = x != 0ull && x >= thmax;
+            const int p = warp_append(&sm.sel.nhi, h);
+            if (h) sm.sortbuf[p] = x;
+          }
+          bar512();
+          const int n_ge = sm.sel.nge;
+          // No CTA left out a key above the k-th candidate: the pool holds the
+          // session's top-k.  (One CTA: its candidates always do.)
+          const bool fast = !overflow && (Gs == 1 || (n_all < k ? thmax == 0ull : n_ge >= k));
+          if (fast) {
+            // Every winner is one of some CTA's candidates at or above the
+            // largest bound, and a candidate wins iff fewer than k pool keys
+            // are above it; its rank is that count.
+            const int nhi = sm.sel.nhi;
+            const int nwin = min(n_all, k);
+            if (nhi <= kDirect) {
+              // per-warp partial counts, in the histogram's words (unused on this path)
+              int *rank_part = reinterpret_cast<int *>(sm.hist);
+              static_assert((kSelThreads / 32) * kDirect <= kHistWords, "rank partials fit the histogram words");
+              for (int e0 = 0; e0 < nhi; e0 += kRankStep) {
+                unsigned long long x[kRankStep];
+                unsigned r[kRankStep];
+  #pragma unroll
+                for (int j = 0; j < kRankStep; ++j) {
+                  x[j] = e0 + j < nhi ? sm.sortbuf[e0 + j] : ~0ull;
+                  r[j] = 0u;
+                }
+  #pragma unroll
+                for (int q = 0; q < kPoolPer; ++q) {
+                  if (q * kSelThreads >= n_ge) break;
+                  const int i = q * kSelThreads + tid;
+                  const unsigned long long pv = i < n_ge ? pool_s[i] : 0ull;
+  #pragma unroll
+                  for (int j = 0; j < kRankStep; ++j) r[j] += pv > x[j] ? 1u : 0u;
+                }
+  #pragma unroll
+                for (int j = 0; j < kRankStep; ++j) r[j] = __reduce_add_sync(0xffffffffu, r[j]);
+                unsigned mine = 0u;
+  #pragma unroll
+                for (int j = 0; j < kRankStep; ++j) mine = lane == j ? r[j] : mine;
+                if (lane < kRankStep && e0 + lane < nhi) rank_part[warp * kDirect + e0 + lane] = int(mine);
+              }
+              bar512();
+              for (int e = tid; e < nhi; e += kSelThreads) {
+                int r = 0;
+  #pragma unroll
+                for (int w = 0; w < kSelThreads / 32; ++w) r += rank_part[w * kDirect + e];
+                if (r < k) {
+                  const unsigned long long x = sm.sortbuf[e];
+                  out_idx[r] = key_index(x);
+                  if (out_score) out_score[r] = key_score(x);
                 }
               }
-              const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
-              const unsigned long long srt = block_sort512_desc(tid < m ? sm.out[tid] : 0ull, sm.sortbuf, tid);
-              if (tid < k) {
-                if (tid < m) {
-                  out_idx[tid] = key_index(srt);
-                  if (out_score) out_score[tid] = key_score(srt);
-                } else {
-                  out_idx[tid] = -1;
-                  if (out_score) out_score[tid] = __uint_as_float(0x7fc00000u);
+            } else {
+              // more candidates: a counting sort of the kept pool keys ranks them all at once
+              uint32_t mn = ~0u, mx = 0u;
+              for (int w = 0; w < kSelThreads / 32; ++w) {
+                mn = min(mn, sm.sel.red_lo[w]);
+                mx = max(mx, sm.sel.red_hi[w]);
+              }
+              const unsigned long long lo = static_cast<unsigned long long>(mn) << 32;
+              const unsigned long long hi = (static_cast<unsigned long long>(mx) << 32) | 0xffffffffull;
+              static_assert(2 * kPoolCap * 8 <= kStages * kStageBytes, "the pool and its sorted copy fit the stage ring");
+              bucket_rank(pool_s, n_ge, sm.sortbuf, nhi, lo, hi, k, sm.hist, pool_s + kPoolCap, sm.sel, tid, out_idx,
+                          out_score);
+            }
+            if (int(blockIdx.x) == cta0) {
+              for (int e = nwin + tid; e < k; e += kSelThreads) {
+                out_idx[e] = -1;
+                if (out_score) out_score[e] = __uint_as_float(0x7fc00000u);
+              }
+            }
+          } else {
+            // ---- exact fallback -----------------------------------------------------
+            // A CTA whose bound is above the k-th candidate may hold winners it
+            // did not publish: it publishes its local top-k below its bound, and
+            // the session's first CTA merges them with the pool.
+            bool flagged;
+            if (overflow || n_all < k) {
+              flagged = th != 0ull;
+            } else {
+              unsigned c = 0u;
+  #pragma unroll
+              for (int q = 0; q < kPoolPer; ++q) {  // the whole pool again (pool_s keeps only the top part)
+                const int i = tid + q * kSelThreads;
+                const unsigned long long pv = i < n_all ? (Gs > 1 ? ld_cg(pool_g + i) : sm.cand[i]) : 0ull;
+                c += (pv != 0ull && pv >= th) ? 1u : 0u;
+              }
+              c = __reduce_add_sync(0xffffffffu, c);
+              bar512();
+              if (lane == 0) sm.sel.red_cnt[warp] = int(c);
+              bar512();
+              int s = 0;
+              for (int w = 0; w < kSelThreads / 32; ++w) s += sm.sel.red_cnt[w];
+              flagged = s < k;
+            }
+            int npub = 0;
+            if (flagged) {
+              const int m = select_top(sm.keys, n_in, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+              for (int i0 = 0; i0 < m; i0 += kSelThreads) {
+                const int i = i0 + tid;
+                const unsigned long long x = i < m ? sm.out[i] : 0ull;
+                const bool pub = x != 0ull && x < th;
+                const int p = warp_append(&sm.sel.pub_cnt, pub);
+                if (pub && p < kPubCap) ws->lists[blockIdx.x][p] = x;
+              }
+              bar512();
+              npub = min(sm.sel.pub_cnt, kPubCap);
+            }
+            if (tid == 0) ws->cnt[blockIdx.x] = npub;
+            bar512();
+            if (tid == 0) red_release_add(&ss.fb[par], 1ull << 32);
+            if (int(blockIdx.x) == cta0) {
+              if (tid == 0) {
+                unsigned long long seen = 0ull;
+                sm.sel.ok = wait_arrivals(&ss.fb[par], unsigned(Gs), hdr, &seen) ? 1 : 0;
+                atomicAdd(&hdr->fallback, 1u);
+              }
+              bar512();
+              if (sm.sel.ok) {
+                // the pool and every flagged CTA's list, reduced to the exact top-k
+                int fill = 0;
+                for (int src_i = -1; src_i < Gs; ++src_i) {
+                  const unsigned long long *src = src_i < 0 ? pool_g : ws->lists[cta0 + src_i];
+                  const int len = src_i < 0 ? (Gs > 1 ? n_all : 0) : min(__ldcg(&ws->cnt[cta0 + src_i]), kPubCap);
+                  for (int off = 0; off < len; off += kPubCap) {
+                    const int cl = min(kPubCap, len - off);
+                    if (fill + cl > kKeysCap) {
+                      const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+                      for (int i = tid; i < m; i += kSelThreads) sm.keys[i] = sm.out[i];
+                      bar512();
+                      fill = m;
+                    }
+                    for (int i = tid; i < cl; i += kSelThreads) sm.keys[fill + i] = ld_cg(src + off + i);
+                    fill += cl;
+                    bar512();
+                  }
+                }
+                const int m = select_top(sm.keys, fill, k, sm.out, sm.hist, sm.sortbuf, sm.sel, tid);
+                const unsigned long long srt = block_sort512_desc(tid < m ? sm.out[tid] : 0ull, sm.sortbuf, tid);
+                if (tid < k) {
+                  if (tid < m) {
+                    out_idx[tid] = key_index(srt);
+                    if (out_score) out_score[tid] = key_score(srt);
+                  } else {
+                    out_idx[tid] = -1;
+                    if (out_score) out_score[tid] = __uint_as_float(0x7fc00000u);
+                  }
                 }
               }
             }
