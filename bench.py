@@ -677,7 +677,7 @@ def run_prefill(args):
     per-query sparse attention."""
     torch, B, dev, stream = _gpu_setup()
     T, n, base = 2048, 65536, 63488
-    per_launch = min(torch.cuda.get_device_properties(dev).multi_processor_count, 256)  # sessions per scorer launch
+    per_launch = min(2 * torch.cuda.get_device_properties(dev).multi_processor_count, 512)  # query tokens per launch
     gen = torch.Generator(device=dev)
     gen.manual_seed(4004)
     with torch.cuda.stream(stream):
@@ -692,7 +692,7 @@ def run_prefill(args):
         scales = torch.empty((T, 64, 4), dtype=torch.uint8, device=dev)
         oi = torch.empty((T, K_TOP), dtype=torch.int32, device=dev)
         out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device=dev)
-        ws_s = torch.empty(B.ds4x_index_score_topk_prefill_workspace(T, K_TOP), dtype=torch.uint8, device=dev)
+        ws_s = torch.empty(B.ds4x_index_score_topk_prefill_workspace(n, T, K_TOP), dtype=torch.uint8, device=dev)
         ws_a = torch.empty(B.ds4x_sparse_attn_decode_workspace(K_TOP), dtype=torch.uint8, device=dev)
         B.ds4x_workspace_init(ws_s, stream=stream)
         B.ds4x_workspace_init(ws_a, stream=stream)
@@ -749,9 +749,9 @@ def run_prefill(args):
                      "peak": peak_fp8, "unit": "TFLOP/s", "frac": flop_score / (parts["score"] * 1e-3) / 1e12 / peak_fp8,
                      "peak_kind": "measured bf16 burst x 2 (FP8 nominal ratio)", "traffic": None,
                      "attention_tflops": flop_attn / (parts["attend"] * 1e-3) / 1e12},
-        # per step: the quantiser, the prefill set-up kernel, one scorer launch per
-        # SM-count query tokens (one session per CTA), and one attention launch
-        "gpu_launches": steps * (3 + (T + per_launch - 1) // per_launch), "clocks": clk.summary()}), flush=True)
+        # per step: the quantiser, a score and a top-k kernel per launch of up to
+        # 2 x SMs query tokens (a pair per CTA), and one attention launch
+        "gpu_launches": steps * (2 + 2 * ((T + per_launch - 1) // per_launch)), "clocks": clk.summary()}), flush=True)
 
 if __name__ == "__main__":
     main()

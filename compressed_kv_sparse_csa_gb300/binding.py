@@ -53,7 +53,7 @@ _SIGNATURES = {
     "ds4x_sparse_attn_prefill": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p,
                                                  _c_size, _c_p]),
     "ds4x_quantize_query_e4m3": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p]),
-    "ds4x_index_score_topk_prefill_workspace": (_c_size, [_c_i32, _c_i32]),
+    "ds4x_index_score_topk_prefill_workspace": (_c_size, [_c_i64, _c_i32, _c_i32]),
     "ds4x_index_score_topk_prefill": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_i32, _c_i64, _c_i32, _c_p, _c_p,
                                                       _c_p, _c_size, _c_p]),
 }
@@ -362,8 +362,8 @@ def ds4x_quantize_query_e4m3(q, codes, scales, stream=None):
     _call("ds4x_quantize_query_e4m3", _ptr(q), n, _ptr(codes), _ptr(scales), _stream(stream))
 
 
-def ds4x_index_score_topk_prefill_workspace(n_queries: int, k: int) -> int:
-    return lib().ds4x_index_score_topk_prefill_workspace(int(n_queries), int(k))
+def ds4x_index_score_topk_prefill_workspace(n_rows: int, n_queries: int, k: int) -> int:
+    return lib().ds4x_index_score_topk_prefill_workspace(int(n_rows), int(n_queries), int(k))
 
 
 def ds4x_index_score_topk_prefill(idx_rows, n_rows, q_codes, q_scales, w, n_queries, causal_base, k, out_idx,

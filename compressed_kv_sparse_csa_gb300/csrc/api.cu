@@ -286,9 +286,9 @@ int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, u
   return from_cuda(launch_quantize_query(q, n_vec128, codes, scales, stream));
 }
 
-size_t ds4x_index_score_topk_prefill_workspace(int32_t n_queries, int32_t k) {
+size_t ds4x_index_score_topk_prefill_workspace(int64_t n_rows, int32_t n_queries, int32_t k) {
   (void)k;
-  return prefill_ws_bytes(n_queries);
+  return prefill_ws_bytes(n_rows, n_queries);
 }
 
 int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
@@ -304,7 +304,7 @@ int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const
   if (n_rows < 1 || n_rows > int64_t(INT32_MAX) || n_queries < 1 || n_queries > DS4X_PREFILL_MAX_QUERIES ||
       k < 1 || k > DS4X_TOPK_MAX)
     return DS4X_EINVAL;
-  if (ws_bytes < ds4x_index_score_topk_prefill_workspace(n_queries, k)) return DS4X_EWORKSPACE;
+  if (ws_bytes < ds4x_index_score_topk_prefill_workspace(n_rows, n_queries, k)) return DS4X_EWORKSPACE;
   const int a = check_arch();
   if (a != DS4X_OK) return a;
   return from_cuda(launch_score_prefill(idx_rows, n_rows, q_codes, q_scales, w, n_queries, causal_base, k, out_idx,

@@ -164,7 +164,9 @@ cudaError_t launch_window_attn(const uint8_t *kv_rows, int64_t n_rows, const int
 // Chunked prefill: query quantiser and the multi-query scorer.
 cudaError_t launch_quantize_query(const float *q, int64_t n_vec, uint8_t *codes, uint8_t *scales,
                                   cudaStream_t stream);
-size_t prefill_ws_bytes(int32_t T);
+// Workspace of the prefill scorer: the header, then the fp32 scores of up to
+// 512 query tokens (one launch's) over n_rows rows.
+size_t prefill_ws_bytes(int64_t n_rows, int32_t T);
 cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
                                  const uint8_t *q_scales, const float *w, int32_t T, int64_t causal_base,
                                  int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream);

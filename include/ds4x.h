@@ -281,21 +281,24 @@ int ds4x_quantize_query_e4m3(const float *q, int64_t n_vec128, uint8_t *codes, u
  *   s_it = sum_h w[i][h] * max(0, q^[i][h] . k_t),  q^ = E4M3 code * 2^(scale-127)
  *
  * and gets the exact top-k of its visible rows (score descending, lower
- * index first; -1 / NaN past its visible count).  Run as the fused scorer
- * over one "session" per query token (one per SM per launch).
+ * index first; -1 / NaN past its visible count).  Runs as launches of up to
+ * 2 x (SM count) query tokens: a tensor-core contraction that streams the
+ * key tiles once per pair of tokens (one block-scaled MMA over both tokens'
+ * 64 heads) and writes their fp32 scores into the workspace, then one
+ * exact top-k per token over those scores.
  *
  *   idx_rows   u8 [n_rows][68]
  *   q_codes    u8 [n_queries][64][128], q_scales u8 [n_queries][64][4]
- *              (ds4x_quantize_query_e4m3); scale bytes 4..245 keep q^
- *              exact in the kernel's bf16 staging
+ *              (ds4x_quantize_query_e4m3; any scale byte 0..254)
  *   w          f32 [n_queries][64]
  *   out_idx    i32 [n_queries][k]; out_score f32 [n_queries][k] or NULL
- *   ws         >= ds4x_index_score_topk_prefill_workspace(n_queries, k)
- *              bytes, zero-filled before first use
+ *   ws         >= ds4x_index_score_topk_prefill_workspace(n_rows, n_queries, k)
+ *              bytes (the 256-byte status header, then the fp32 scores of
+ *              up to 512 tokens over n_rows rows), zero-filled before first use
  *
  * Errors: DS4X_EINVAL (pointers, sizes, k), DS4X_EWORKSPACE.
  */
-size_t ds4x_index_score_topk_prefill_workspace(int32_t n_queries, int32_t k);
+size_t ds4x_index_score_topk_prefill_workspace(int64_t n_rows, int32_t n_queries, int32_t k);
 int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
                                   const uint8_t *q_scales, const float *w, int32_t n_queries, int64_t causal_base,
                                   int32_t k, int32_t *out_idx, float *out_score, void *ws, size_t ws_bytes,

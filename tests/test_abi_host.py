@@ -126,7 +126,7 @@ def test_prefill_scorer_argument_checks(lib):
     assert f(FAKE, 0, FAKE, FAKE, None) == -1
     assert f(FAKE, 4, FAKE + 4, FAKE, None) == -1
     g = lib.ds4x_index_score_topk_prefill
-    ws = lib.ds4x_index_score_topk_prefill_workspace(2048, 512)
+    ws = lib.ds4x_index_score_topk_prefill_workspace(65536, 2048, 512)
     assert ws >= 2048 * 64 * 128 * 2
     assert g(None, 65536, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws, None) == -1
     assert g(FAKE, 0, FAKE, FAKE, FAKE, 2048, 63488, 512, FAKE, None, FAKE, ws, None) == -1

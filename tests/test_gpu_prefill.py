@@ -58,7 +58,7 @@ def test_prefill_topk_parity(T, n, base, k):
     codes, scales = P.quantize_query_e4m3(case["q"])
     out_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     out_score = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    ws = new_ws(B.ds4x_index_score_topk_prefill_workspace(T, k))
+    ws = new_ws(B.ds4x_index_score_topk_prefill_workspace(n, T, k))
     B.ds4x_index_score_topk_prefill(idx_rows, n, dev(codes), dev(scales), dev(case["w"]), T, base, k, out_idx,
                                     out_score, ws)
     torch.cuda.synchronize()
@@ -70,3 +70,61 @@ def test_prefill_topk_parity(T, n, base, k):
         vis = int(np.sum(np.isfinite(s[i])))
         assert vis == min(n, base + i)
         check_topk(gi[i], gs[i], s[i, :vis], k)
+
+
+def _score_prefill(idx_rows, n, codes, scales, w, T, base, k):
+    B = require_gpu()
+    out_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out_score = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = new_ws(B.ds4x_index_score_topk_prefill_workspace(n, T, k))
+    B.ds4x_index_score_topk_prefill(idx_rows, n, dev(codes), dev(scales), dev(w), T, base, k, out_idx, out_score, ws)
+    torch.cuda.synchronize()
+    assert B.ds4x_workspace_status(ws) == 0
+    return out_idx.cpu().numpy(), out_score.cpu().numpy()
+
+
+def test_prefill_all_scores_equal_lowest_rows_win():
+    """20,000 copies of one row: every visible score of a query is the same,
+    more than the top-k kernel holds in shared memory, so the tie is broken
+    by the index-order pass: rows 0..k-1 exactly."""
+    require_gpu()
+    n, T, base, k = 20000, 5, 19998, 512
+    case = prefill_case(T=T, n=1, causal_base=0)
+    idx_in = np.tile(case["idx_in"][:1], (n, 1))
+    idx_rows, _ = pack(idx_in=idx_in)
+    codes, scales = P.quantize_query_e4m3(case["q"])
+    gi, gs = _score_prefill(idx_rows, n, codes, scales, case["w"], T, base, k)
+    s = P.prefill_scores(C.pack_idx_rows(idx_in[:1]), codes, scales, case["w"], 1)[:, 0]
+    for i in range(T):
+        assert np.array_equal(gi[i], np.arange(k)), i
+        assert np.all(gs[i] == gs[i, 0])
+        np.testing.assert_allclose(gs[i, 0], s[i], rtol=2e-5)
+
+
+def test_prefill_one_hot_queries_wide_buckets():
+    """One-hot queries (code 1.0 at one element of one head, one-hot weights):
+    every score is one E2M1 key value times a power of two, so thousands of
+    rows share the k-th score; the histogram passes narrow to it and the
+    index-order pass breaks the tie.  The scores are exact in fp32, so the
+    lists must equal the oracle's, order included."""
+    require_gpu()
+    n, T, base, k = 30000, 6, 29995, 512
+    case = prefill_case(T=T, n=n, causal_base=base)
+    idx_rows, _ = pack(idx_in=case["idx_in"])
+    codes = np.zeros((T, 64, 128), dtype=np.uint8)
+    scales = np.full((T, 64, 4), 127, dtype=np.uint8)
+    w = np.zeros((T, 64), dtype=np.float32)
+    for i in range(T):
+        h, e = (5 * i + 3) % 64, (37 * i + 11) % 128
+        codes[i, h, e] = 0x38  # 1.0
+        w[i, h] = 1.0 if i % 2 == 0 else 0.25
+        if i == 3:  # a negative weight: most scores zero or below
+            w[i, h] = -1.0
+    gi, gs = _score_prefill(idx_rows, n, codes, scales, w, T, base, k)
+    rows = C.pack_idx_rows(case["idx_in"])
+    o_idx, o_val, s = P.prefill_topk(rows, codes, scales, w, base, k)
+    for i in range(T):
+        vis = min(n, base + i)
+        check_topk(gi[i], gs[i], s[i, :vis], k)
+        assert np.array_equal(gi[i], o_idx[i]), i
+        assert np.array_equal(gs[i].astype(np.float64), o_val[i]), i

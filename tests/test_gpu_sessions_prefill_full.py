@@ -9,7 +9,8 @@
   vector; the per-query exact top-512 of every query computed on the GPU and
   checked for a seeded sample of 32 queries (the first and the last among
   them); the per-query attention over the GPU's lists for the same sample.
-  Every query's visible range spans about 3.3 tiles per CTA.
+  Each score CTA streams a query pair's ~496 visible tiles, and each query's
+  top-k runs over ~64K scores: the histogram passes, not the in-memory path.
 """
 
 import numpy as np
@@ -88,7 +89,7 @@ def test_prefill_chunk_2048_queries_65536_rows():
 
     out_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     out_score = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    ws = new_ws(B.ds4x_index_score_topk_prefill_workspace(T, k))
+    ws = new_ws(B.ds4x_index_score_topk_prefill_workspace(n, T, k))
     B.ds4x_index_score_topk_prefill(idx_rows, n, codes, scales, dev(case["w"]), T, base, k, out_idx, out_score, ws)
     out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device="cuda")
     ws_a = new_ws(B.ds4x_sparse_attn_decode_workspace(k))
