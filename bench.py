@@ -72,7 +72,7 @@ def measured_peak():
 # Source files each timed kernel is built from: an ncu traffic figure is
 # reported only while these are unchanged since the capture.
 KERNEL_SOURCES = {
-    "ds4x_index_score_topk": ("score_fused.cu", "tc_ptx.cuh", "ds4x_internal.cuh"),
+    "ds4x_index_score_topk": ("score_fused.cu", "select512.cuh", "tc_ptx.cuh", "ds4x_internal.cuh"),
     "ds4x_sparse_attn_decode": ("attn_decode.cu", "ds4x_internal.cuh"),
 }
 
