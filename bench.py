@@ -18,8 +18,9 @@ over the whole job; `roofline` is the dominant kernel (the scorer entry
 point) timed on its own over K graph replays; `e2e` times the same step
 through the public API from pinned host buffers (append of the new row,
 score, attention, result copied back); `cpu_baseline` is the float64 oracle
-on the host cores on a bounded sample.  `--impl reference` times the oracle
-alone (rank 0 only).
+on the host cores (all cores over the whole workload; one core on a
+262,144-row sample).  `--impl reference` times the oracle alone over the
+whole workload on all host cores (rank 0 only).
 """
 
 from __future__ import annotations
@@ -39,7 +40,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode attn step latency (µs/layer) & compressed rows/s vs N; achieved HBM GB/s"
 WORKLOADS = {"tiny": 4096, "mid": 131072, "long": 1048576}
-EXTRA_WORKLOADS = ("sessions", "prefill", "hca")  # parity configurations, measured on request
+EXTRA_WORKLOADS = ("sessions", "prefill", "hca", "window")  # parity configurations, measured on request
 K_TOP = 512
 HEADS = 64
 FALLBACK_HBM_GBS = 6800.0
@@ -191,12 +192,103 @@ def run_oracle_subprocess(n_rows, reps):
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+
+    return platform.machine()
+
+
+def _oracle_score_chunk(task):
+    """Pool worker: the oracle's scores of rows [a, b) of the shared packed rows."""
+    from multiprocessing import shared_memory
+
+    import numpy as np
+
+    from oracle import indexer as I
+
+    name, n, a, b, q_bits, w = task
+    shm = shared_memory.SharedMemory(name=name)
+    try:
+        rows = np.ndarray((n, 68), dtype=np.uint8, buffer=shm.buf)
+        return a, I.score_rows(rows[a:b], q_bits, w)
+    finally:
+        shm.close()
+
+
+def oracle_step_all_cores(n_rows=1048576, reps=3, seed=1002, all_steps=False):
+    """The oracle's decode step over every row of the long-decode workload on
+    all host cores: the unchanged oracle scorer on one chunk of rows per
+    process (one BLAS thread each, a spawn pool started before the timing),
+    then the oracle's top-512 and attention in this process.  Returns
+    (seconds per step, processes)."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+
+    import numpy as np
+
+    from oracle import codecs as C
+    from oracle import indexer as I
+    from oracle.attention import sparse_attn_decode
+    from synth import decode_case
+
+    procs = os.cpu_count() or 1
+    case = decode_case(n_rows, seed)
+    rows = C.pack_idx_rows(case["idx_in"])  # the cache contents (not timed)
+    shm = shared_memory.SharedMemory(create=True, size=rows.nbytes)
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    try:
+        np.ndarray(rows.shape, dtype=np.uint8, buffer=shm.buf)[:] = rows
+        for k in saved:
+            os.environ[k] = "1"  # inherited by the spawned workers
+        bounds = np.linspace(0, n_rows, 4 * procs + 1).astype(np.int64)
+        tasks = [(shm.name, n_rows, int(a), int(b), case["q_idx"], case["w"]) for a, b in zip(bounds[:-1], bounds[1:])]
+        secs = []
+        with mp.get_context("spawn").Pool(procs) as pool:
+            pool.map(_oracle_score_chunk, tasks[:procs])  # start-up and imports, not timed
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                parts = pool.map(_oracle_score_chunk, tasks)
+                s = np.concatenate([p for _, p in sorted(parts, key=lambda x: x[0])])
+                idx, _ = I.topk(s, K_TOP)
+                t1 = time.perf_counter()
+                kv_sel = C.pack_kv_rows(case["kv_in"][idx])  # packing is not part of the step
+                t2 = time.perf_counter()
+                sparse_attn_decode(kv_sel, np.arange(idx.shape[0]), case["q_attn"], 1.0 / math.sqrt(512.0))
+                secs.append((t1 - t0) + (time.perf_counter() - t2))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        shm.close()
+        shm.unlink()
+    if all_steps:
+        return secs, procs
+    return sorted(secs)[len(secs) // 2], procs
+
+
 def cpu_baseline(n_rows=262144, reps=5):
     secs = run_oracle_subprocess(n_rows, reps)
-    t = sorted(secs)[len(secs) // 2]
-    return {"value": n_rows / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"median of {reps} oracle steps (score + top-512 + attention) over {n_rows} rows of the "
-                      f"long-decode distribution, numpy float64, 1 thread; {t:.2f} s each"}
+    t1 = sorted(secs)[len(secs) // 2]
+    n_all = WORKLOADS["long"]
+    t_all, procs = oracle_step_all_cores(n_all)
+    return {"value": n_all / t_all, "unit": "rows/s", "cores": procs, "kind": "oracle",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "sample": f"median of 3 oracle steps (score + top-512 + attention) over all {n_all} rows of the "
+                      f"long-decode workload, numpy float64, the unchanged oracle scorer on {procs} processes "
+                      f"(one per core, one BLAS thread each), top-512 and attention in one; {t_all:.2f} s each",
+            "single_thread": {"value": n_rows / t1, "unit": "rows/s", "cores": 1,
+                              "sample": f"median of {reps} oracle steps over {n_rows} rows of the same "
+                                        f"distribution, 1 thread; {t1:.2f} s each"}}
 
 
 def max_over_ranks(values, dist, device):
@@ -217,26 +309,26 @@ def job_value(world, n_rows, ms_per_step):
 
 
 def reference_arm(args, workload, n):
+    """The oracle (the only other implementation of the path) on the host's
+    cores: every step is the oracle's score + top-512 + attention over all n
+    rows of the workload, the scorer on one process per core."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    # size each step's sample so the whole run stays within about two minutes
-    probe = run_oracle_subprocess(8192, 1)[0]
-    rate = 8192 / probe
-    total_steps = args.steps + args.warmup
-    sample = int(max(1024, min(262144, rate * 100.0 / max(1, total_steps))) // 1024 * 1024)
-    secs = run_oracle_subprocess(sample, total_steps)
+    secs, procs = oracle_step_all_cores(n, reps=args.warmup + args.steps, seed=1000 + list(WORKLOADS).index(workload),
+                                        all_steps=True)
     timed = secs[args.warmup:]
     t = sum(timed)
-    value = sample * len(timed) / t
+    value = n * len(timed) / t
+    sample = (f"all {n} rows of the {workload} decode workload per step, numpy float64 oracle, the scorer "
+              f"on {procs} processes (one per core), top-512 and attention in one; host CPU {cpu_model()}")
     line = {"metric": METRIC, "value": value, "unit": "compressed rows/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload, "n_rows": n, "top_k": K_TOP, "sample_rows_per_step": sample},
-            "cpu_baseline": {"value": value, "unit": "compressed rows/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{sample} rows per step of the {workload} decode distribution, "
-                                       "numpy float64 oracle, 1 thread"},
+            "config": {"workload": workload, "n_rows": n, "top_k": K_TOP},
+            "cpu_baseline": {"value": value, "unit": "compressed rows/s", "cores": procs, "kind": "oracle",
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "compressed rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -261,7 +353,7 @@ def main():
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode workloads only"}))
             return
-        {"sessions": run_sessions, "prefill": run_prefill, "hca": run_hca}[args.workload](args)
+        {"sessions": run_sessions, "prefill": run_prefill, "hca": run_hca, "window": run_window}[args.workload](args)
         return
     n = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -669,6 +761,67 @@ def run_hca(args):
                      "peak": peak, "unit": "GB/s", "frac": algo / (ms * 1e-3) / 1e9 / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": algo, "peak_kind": kind},
         "gpu_launches": steps * 2, "clocks": clk.summary()}), flush=True)
+
+
+def run_window(args):
+    """Decode attention over the 512 selected rows of a 1,048,576-row cache and
+    all 256 live rows of the layer's raw sliding window, one softmax over
+    both: 8 index lists and 8 rings rotated (the selected rows are random
+    rows of the 611 MB cache, so they come from HBM), one CUDA graph each."""
+    torch, B, dev, stream = _gpu_setup()
+    n, L, w = 1048576, 8, 256
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7007)
+    with torch.cuda.stream(stream):
+        kv = torch.empty(n * 583, dtype=torch.uint8, device=dev)
+        chunk = 1 << 18
+        for a in range(0, n, chunk):
+            B.ds4x_cache_append(kv, None, a, torch.randn((chunk, 512), generator=gen, device=dev), None, stream=stream)
+        items = []
+        for _ in range(L):
+            ring = torch.empty(256 * 583, dtype=torch.uint8, device=dev)
+            B.ds4x_cache_append(ring, None, 0, torch.randn((256, 512), generator=gen, device=dev), None, stream=stream)
+            idx = torch.randperm(n, generator=gen, device=dev)[:K_TOP].to(torch.int32)
+            items.append({"ring": ring, "idx": idx, "q": torch.randn((64, 512), generator=gen, device=dev).to(torch.bfloat16),
+                          "out": torch.empty((64, 512), dtype=torch.bfloat16, device=dev)})
+        ws = torch.empty(B.ds4x_window_sparse_attn_decode_workspace(), dtype=torch.uint8, device=dev)
+        B.ds4x_workspace_init(ws, stream=stream)
+    stream.synchronize()
+    scale = 1.0 / math.sqrt(512.0)
+
+    def step(c):
+        B.ds4x_window_sparse_attn_decode(kv, n, c["idx"], K_TOP, c["ring"], 200, w, c["q"], scale, c["out"], None, ws,
+                                         stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(items[i % L])
+    stream.synchronize()
+    graphs = []
+    for c in items:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    steps = min(args.steps, 2000)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        ms = _timed_graph(torch, stream, graphs, steps, args.warmup)
+    peak, kind = measured_peak()
+    # the selected and the window rows, the index list, the query, the output
+    algo = (K_TOP + w) * 583 + K_TOP * 4 + 2 * 64 * 512 * 2
+    print(json.dumps({
+        "metric": "sparse + sliding-window decode attention latency (us)",
+        "value": ms * 1e3, "unit": "us/call", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-in/fp32-acc (E4M3/FP16 packed rows)", "data": "synthetic",
+        "config": {"workload": "512 selected rows of a 1,048,576-row cache + 256 live raw-window rows, 64 heads",
+                   "n_rows": n, "window": w, "rotated": L,
+                   "l2": "selected rows random over a 611 MB cache (above L2); 8 rings and index lists rotated"},
+        "roofline": {"kernel": "ds4x_window_sparse_attn_decode", "bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": algo / (ms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": algo, "peak_kind": kind},
+        # per call: the index-list set-up kernel, the attention over the two items, the finalize
+        "gpu_launches": steps * 3, "clocks": clk.summary()}), flush=True)
 
 
 def run_prefill(args):
