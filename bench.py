@@ -400,18 +400,19 @@ def main():
                            "out_score": torch.empty(K_TOP, dtype=torch.float32, device=dev),
                            "out": torch.empty((HEADS, 512), dtype=torch.bfloat16, device=dev)})
         ws_s = torch.empty(B.ds4x_index_score_topk_workspace(n, K_TOP), dtype=torch.uint8, device=dev)
-        ws_a = torch.empty(B.ds4x_sparse_attn_decode_workspace(K_TOP), dtype=torch.uint8, device=dev)
+        ws_d = torch.empty(B.ds4x_csa_decode_step_workspace(n, K_TOP), dtype=torch.uint8, device=dev)
         B.ds4x_workspace_init(ws_s, stream=stream)
-        B.ds4x_workspace_init(ws_a, stream=stream)
+        B.ds4x_workspace_init(ws_d, stream=stream)
     stream.synchronize()
 
     def step(l, score_only=False):
         c = layers[l]
-        B.ds4x_index_score_topk(c["idx_rows"], n, c["q_idx"], c["w"], K_TOP, c["out_idx"], c["out_score"], ws_s,
-                                stream=stream)
-        if not score_only:
-            B.ds4x_sparse_attn_decode(c["kv_rows"], n, c["out_idx"], K_TOP, c["q_attn"], scale, c["out"], None,
-                                      ws_a, stream=stream)
+        if score_only:
+            B.ds4x_index_score_topk(c["idx_rows"], n, c["q_idx"], c["w"], K_TOP, c["out_idx"], c["out_score"], ws_s,
+                                    stream=stream)
+        else:  # the decode step: score + top-512, then attention over the selected rows
+            B.ds4x_csa_decode_step(c["idx_rows"], c["kv_rows"], n, c["q_idx"], c["w"], K_TOP, c["q_attn"], scale,
+                                   c["out_idx"], c["out_score"], c["out"], None, ws_d, stream=stream)
 
     # kernels each entry point launches: the fused scorer is one kernel, the
     # two-stage scorer two; attention is one cluster kernel
@@ -501,8 +502,8 @@ def main():
         c = layers[l]
         d_in.copy_(h_in, non_blocking=True)
         B.ds4x_cache_append(c["kv_rows"], c["idx_rows"], n - 1, d_kv, d_idx, stream=stream)
-        B.ds4x_index_score_topk(c["idx_rows"], n, d_q, d_w, K_TOP, d_oidx, c["out_score"], ws_s, stream=stream)
-        B.ds4x_sparse_attn_decode(c["kv_rows"], n, d_oidx, K_TOP, d_qa, scale, d_out, None, ws_a, stream=stream)
+        B.ds4x_csa_decode_step(c["idx_rows"], c["kv_rows"], n, d_q, d_w, K_TOP, d_qa, scale, d_oidx, c["out_score"],
+                               d_out, None, ws_d, stream=stream)
         h_res.copy_(d_res, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -579,7 +580,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": ms_e2e_step,
                 "path": "per step one CUDA graph of the public calls: one pinned-host-to-device copy of the "
-                        "packed inputs, ds4x_cache_append, ds4x_index_score_topk, ds4x_sparse_attn_decode, one "
+                        "packed inputs, ds4x_cache_append, ds4x_csa_decode_step (score + top-512, attention), one "
                         "device-to-pinned-host copy of the output and indices"},
         "gpu_launches": args.steps * (launches_per_step["score"] + launches_per_step["attn"]),
         "clocks": clocks,

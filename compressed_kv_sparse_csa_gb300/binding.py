@@ -45,6 +45,9 @@ _SIGNATURES = {
     "ds4x_checkpoint_load": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32]),
     "ds4x_window_sparse_attn_decode": (ctypes.c_int, [_c_p, _c_i64, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_f32,
                                                       _c_p, _c_p, _c_p, _c_size, _c_p]),
+    "ds4x_csa_decode_step_workspace": (_c_size, [_c_i64, _c_i32]),
+    "ds4x_csa_decode_step": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_f32, _c_p, _c_p, _c_p,
+                                            _c_p, _c_p, _c_size, _c_p]),
     "ds4x_index_score_topk_batched_workspace": (_c_size, [_c_i32, _c_i32]),
     "ds4x_index_score_topk_batched": (ctypes.c_int, [_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size,
                                                       _c_p]),
@@ -301,6 +304,30 @@ def ds4x_sparse_attn_decode_noalloc(kv_rows, n_rows, idx, k, q_bf16, softmax_sca
     _check(lse, torch.float32, "lse", numel=64, allow_none=True)
     _call("ds4x_sparse_attn_decode_noalloc", _ptr(kv_rows), int(n_rows), _ptr(idx), int(k), _ptr(q_bf16),
           float(softmax_scale), _ptr(out_bf16), _ptr(lse), _stream(stream))
+
+
+def ds4x_csa_decode_step_workspace(n_rows: int, k: int) -> int:
+    return lib().ds4x_csa_decode_step_workspace(int(n_rows), int(k))
+
+
+def ds4x_csa_decode_step(idx_rows, kv_rows, n_rows, q_idx_bf16, w, k, q_attn_bf16, softmax_scale, out_idx, out_score,
+                         out_bf16, lse, ws, stream=None):
+    """One decode step: score + exact top-k over idx_rows, then attention of
+    q_attn_bf16 [64, 512] over the selected kv_rows."""
+    n = int(n_rows)
+    _check(idx_rows, torch.uint8, "idx_rows", numel=n * 68)
+    _check(kv_rows, torch.uint8, "kv_rows", numel=n * 583)
+    _check(q_idx_bf16, torch.bfloat16, "q_idx_bf16", numel=64 * 128)
+    _check(w, torch.float32, "w", numel=64)
+    _check(q_attn_bf16, torch.bfloat16, "q_attn_bf16", numel=64 * 512)
+    _check(out_idx, torch.int32, "out_idx", numel=int(k))
+    _check(out_score, torch.float32, "out_score", numel=int(k), allow_none=True)
+    _check(out_bf16, torch.bfloat16, "out_bf16", numel=64 * 512)
+    _check(lse, torch.float32, "lse", numel=64, allow_none=True)
+    _check(ws, torch.uint8, "ws")
+    _call("ds4x_csa_decode_step", _ptr(idx_rows), _ptr(kv_rows), n, _ptr(q_idx_bf16), _ptr(w), int(k),
+          _ptr(q_attn_bf16), float(softmax_scale), _ptr(out_idx), _ptr(out_score), _ptr(out_bf16), _ptr(lse), _ptr(ws),
+          ws.numel(), _stream(stream))
 
 
 def ds4x_index_score_topk_batched_workspace(n_sess: int, k: int) -> int:

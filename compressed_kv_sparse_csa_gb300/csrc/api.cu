@@ -153,6 +153,35 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
                                       ws, stream));
 }
 
+size_t ds4x_csa_decode_step_workspace(int64_t n_rows, int32_t k) {
+  const size_t a = ds4x_index_score_topk_workspace(n_rows, k), b = ds4x_sparse_attn_decode_workspace(k);
+  return a > b ? a : b;
+}
+
+int ds4x_csa_decode_step(const uint8_t *idx_rows, const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q_idx_bf16,
+                         const float *w, int32_t k, const uint16_t *q_attn_bf16, float softmax_scale,
+                         int32_t *out_idx, float *out_score, uint16_t *out_bf16, float *lse, void *ws,
+                         size_t ws_bytes, ds4x_stream_t stream) {
+  if (idx_rows == nullptr || kv_rows == nullptr || q_idx_bf16 == nullptr || w == nullptr || q_attn_bf16 == nullptr ||
+      out_idx == nullptr || out_bf16 == nullptr || ws == nullptr)
+    return DS4X_EINVAL;
+  if (!aligned16(idx_rows) || !aligned16(kv_rows) || !aligned16(q_idx_bf16) || !aligned16(w) ||
+      !aligned16(q_attn_bf16) || !aligned16(out_idx) || !aligned16(out_bf16) || !aligned16(ws) ||
+      (out_score != nullptr && !aligned16(out_score)) || (lse != nullptr && !aligned16(lse)))
+    return DS4X_EINVAL;
+  if (n_rows < 1 || n_rows > int64_t(INT32_MAX) || k < 1 || k > DS4X_TOPK_MAX) return DS4X_EINVAL;
+  if (ws_bytes < ds4x_csa_decode_step_workspace(n_rows, k)) return DS4X_EWORKSPACE;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  // the attention shares the scorer's workspace header (it only ever sets its status word)
+  cudaError_t e = use_two_stage()
+                      ? launch_score_two_stage(idx_rows, n_rows, q_idx_bf16, w, k, out_idx, out_score, ws, stream)
+                      : launch_score_fused(idx_rows, n_rows, q_idx_bf16, w, k, out_idx, out_score, ws, stream);
+  if (e != cudaSuccess) return DS4X_ECUDA;
+  return from_cuda(launch_attn_decode(kv_rows, n_rows, out_idx, k, q_attn_bf16, softmax_scale, out_bf16, lse, ws,
+                                      stream));
+}
+
 size_t ds4x_index_score_topk_batched_workspace(int32_t n_sess, int32_t k) {
   (void)n_sess;
   (void)k;

@@ -215,6 +215,28 @@ int ds4x_sparse_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_
                             ds4x_stream_t stream);
 
 /*
+ * One decode step of a CSA layer in one call: ds4x_index_score_topk
+ * followed by ds4x_sparse_attn_decode over the k rows it selected, on one
+ * stream, with one workspace (the attention is launched as a programmatic
+ * dependent of the scorer, as when the two are called in turn).  The results
+ * are exactly those of the two calls (out_idx / out_score as the scorer's,
+ * out_bf16 / lse as the attention's).
+ *
+ *   idx_rows, n_rows, q_idx_bf16, w, k, out_idx, out_score  as ds4x_index_score_topk
+ *   kv_rows, q_attn_bf16, softmax_scale, out_bf16, lse      as ds4x_sparse_attn_decode
+ *   ws         >= ds4x_csa_decode_step_workspace(n_rows, k) bytes, zero-filled
+ *              before first use; its status word covers both kernels
+ *
+ * Errors: DS4X_EINVAL (pointers, n_rows < 1, k outside 1..512),
+ * DS4X_EWORKSPACE, DS4X_EARCH, DS4X_ECUDA.
+ */
+size_t ds4x_csa_decode_step_workspace(int64_t n_rows, int32_t k);
+int ds4x_csa_decode_step(const uint8_t *idx_rows, const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q_idx_bf16,
+                         const float *w, int32_t k, const uint16_t *q_attn_bf16, float softmax_scale,
+                         int32_t *out_idx, float *out_score, uint16_t *out_bf16, float *lse, void *ws,
+                         size_t ws_bytes, ds4x_stream_t stream);
+
+/*
  * Micro-batched decode: the CSA indexer score + exact top-k of n_sess
  * independent sessions in one launch (the sessions' CTAs are split in
  * proportion to their history lengths; each session is merged by the last

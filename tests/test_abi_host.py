@@ -186,3 +186,24 @@ def test_ring_rows_match_the_pages_allocation():
     text = open(HEADER).read()
     ring = int(re.search(r"#define DS4X_RING_ROWS (\d+)", text).group(1))
     assert 43 * ring * int(g["kv_row_bytes"]) == int(g["alloc_raw_rings"])
+
+
+def test_decode_step_argument_checks(lib):
+    s = ctypes.c_float(0.044)
+    f = lib.ds4x_csa_decode_step
+    ws = lib.ds4x_csa_decode_step_workspace(100000, 512)
+    assert ws >= lib.ds4x_index_score_topk_workspace(100000, 512)
+    assert ws >= lib.ds4x_sparse_attn_decode_workspace(512)
+    ok = (FAKE, FAKE, 100000, FAKE, FAKE, 512, FAKE, s, FAKE, None, FAKE, None, FAKE, ws, None)
+    for i in (0, 1, 3, 4, 6, 8, 10, 12):  # every required pointer
+        args = list(ok)
+        args[i] = None
+        assert f(*args) == -1, i
+    args = list(ok); args[1] = FAKE + 8
+    assert f(*args) == -1  # misaligned
+    args = list(ok); args[2] = 0
+    assert f(*args) == -1
+    args = list(ok); args[5] = 513
+    assert f(*args) == -1
+    args = list(ok); args[13] = ws - 1
+    assert f(*args) == -3
