@@ -249,19 +249,11 @@ int ds4x_sparse_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32
     return DS4X_EINVAL;
   if (n_rows < 1 || n_queries < 1 || n_queries > DS4X_PREFILL_MAX_QUERIES || k < 1 || k > DS4X_TOPK_MAX)
     return DS4X_EINVAL;
-  if (ws_bytes < ds4x_sparse_attn_decode_workspace(k)) return DS4X_EWORKSPACE;
+  if (ws_bytes < ds4x_sparse_attn_decode_workspace(k) || ws_bytes < attn_prefill_ws_bytes()) return DS4X_EWORKSPACE;
   const int a = check_arch();
   if (a != DS4X_OK) return a;
-  AttnBatch ab{};
-  ab.kv = kv_rows;
-  ab.n_rows = n_rows;
-  ab.idx = idx;
-  ab.k = k;
-  ab.scale = softmax_scale;
-  ab.q = q_bf16;
-  ab.out = out_bf16;
-  ab.lse = lse;
-  return from_cuda(launch_attn_batch(ab, n_queries, ws, stream));
+  return from_cuda(launch_attn_prefill(kv_rows, n_rows, idx, n_queries, k, q_bf16, softmax_scale, out_bf16, lse, ws,
+                                       stream));
 }
 
 size_t ds4x_dense_attn_decode_workspace(int64_t n_rows) {

@@ -170,6 +170,12 @@ size_t prefill_ws_bytes(int64_t n_rows, int32_t T);
 cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const uint8_t *q_codes,
                                  const uint8_t *q_scales, const float *w, int32_t T, int64_t causal_base,
                                  int32_t k, int32_t *out_idx, float *out_score, void *ws, cudaStream_t stream);
+// Prefill attention on the tensor cores: n_queries query tokens, each over its
+// own k selected rows (idx [n_queries][k]), one persistent CTA per SM.
+size_t attn_prefill_ws_bytes();
+cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
+                                int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
+                                cudaStream_t stream);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                int32_t k, const uint16_t *q, float scale, uint16_t *out,
                                float *lse, void *ws, cudaStream_t stream);

@@ -1,7 +1,7 @@
-// Thin inline-PTX wrappers for the sm_103a features the fused scorer uses:
-// mbarriers, 1-D bulk (TMA) copies, tensor memory (tcgen05.alloc/ld/st),
-// block-scaled tcgen05.mma with the A operand in tensor memory, and named
-// barriers.
+// Thin inline-PTX wrappers for the sm_103a features the tensor-core kernels
+// use: mbarriers, 1-D bulk (TMA) copies, tensor memory (tcgen05.alloc/ld/st),
+// block-scaled tcgen05.mma with the A operand in tensor memory, fp16
+// tcgen05.mma with both operands in shared memory, and named barriers.
 #pragma once
 
 #include <stdint.h>
@@ -200,6 +200,49 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over its nthreads participants:
+// every participant gets the same result.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %3, 0;\n\tbar.red.or.pred q, %1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(uint32_t(v))
+      : "memory");
+  return r != 0;
+}
+
+// ---- kind::f16 (fp16 operands, fp32 accumulate) --------------------------------
+// Instruction descriptor: D f32 (bits 4-5 = 1), A and B fp16 (type 0), A / B
+// K-major (0) or MN-major (1) in bits 15 / 16, N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D (+)= A * B with A and B in shared memory (descriptors); accumulate when acc != 0.
+// With no swizzle the descriptor's leading byte offset is the distance between
+// core matrices adjacent along K and the stride byte offset the distance along
+// M (or N), for K-major and MN-major operands alike.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: this thread's lane, columns taddr..taddr+15.
+__device__ __forceinline__ void tc_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 
 }  // namespace ptx
