@@ -15,10 +15,13 @@
 //   S^T[128 rows][64 heads] = V'[128 rows][512] . Q'[64 heads][512]^T
 //   O^T[512 dims][64 heads] += V'^T[512][128 rows] . P^T[128 rows][64 heads]
 //
-// V' is the tile's rows widened to fp16 once, in shared memory, in the
-// canonical no-swizzle layout (core matrices of 8 rows x 8 dims); the first
-// MMA reads it K-major (rows = M), the second reads the same bytes MN-major
-// (dims = M), so each row is widened once and read twice.
+// V' is the tile's rows widened to fp16 once, in shared memory, as eight
+// 128-byte-swizzled panels of 64 dims (row r of a panel: 128 bytes, its
+// 16-byte chunk c at position c ^ (r % 8)).  The first MMA reads the panels
+// K-major (rows = M, a K step 32 bytes further into a panel), the second
+// reads the same bytes MN-major (dims = M: two panels per 128-dim M tile),
+// so each row is widened once and read twice.  Q' and P^T use the same
+// swizzle.
 //
 // Exact operands.  Before a query's first tile its S_b (b < 7) = the largest
 // scale byte of non-RoPE block b over the query's selected rows is found.
@@ -37,17 +40,17 @@
 // p = 2^(l - m) stays below 2^8.  p goes to the second MMA as fp16 hi + lo
 // (22 significant bits); the running sums are fp32.
 //
-// Roles: all 16 warps widen each tile's rows (two passes of 64 rows, eight
-// threads per row: seven 8-dim non-RoPE chunks and one RoPE chunk each,
-// straight from global memory with 4-byte loads), then read S^T (warp w:
+// Roles: all 16 warps widen (warp w: rows 8 w .. 8 w + 7 of each tile, one
+// row per step, lane L converting the row's 4-byte words L + 32 i:
+// coalesced loads, conflict-free swizzled stores), then read S^T (warp w:
 // lanes 32 (w % 4) .., heads 16 (w / 4) ..), run the softmax and write P^T;
 // thread 0 issues each tile's MMAs once a barrier shows every warp's
-// operands written.  One tile's steps run in sequence: widen -> S^T ->
-// softmax -> O^T, the next tile's widening waiting for the previous tile's
-// second MMA to release V' and P^T.
+// operands written.  A tile's steps run in sequence: widen -> S^T ->
+// softmax -> O^T; the next tile's row words are requested as soon as this
+// tile's second MMA is issued, so they arrive while it runs.
 //
 // Named barriers: 1 = vote (bar.red.or of a failed wait, so that all threads
-// leave together), 2 = the tile maxima, 3 = the S_b reset.
+// leave together), 2 = the tile maxima.
 //
 // Every wait is bounded (0.5 s); a time-out sets DS4X_ETIMEOUT in the
 // workspace status and every thread leaves at its next vote.
@@ -62,33 +65,48 @@ namespace {
 using namespace ptx;
 
 constexpr int kHeads = 64;
-constexpr int kDim = DS4X_KV_DIM;                     // 512
+constexpr int kDim = DS4X_KV_DIM;                          // 512
 constexpr int kNopeBlocks = DS4X_KV_NOPE / DS4X_KV_BLOCK;  // 7
-constexpr int kTile = 128;                            // rows per tile
-constexpr int kWorkers = 512;                         // warps 0-15
-constexpr int kThreads = kWorkers;
+constexpr int kTile = 128;                                 // rows per tile
+constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kOCol = 0;                         // O^T: dims 128 i .. as columns 64 i .. 64 i + 63
-constexpr uint32_t kSCol = 256;                       // S^T: columns 256 .. 319
+constexpr uint32_t kOCol = 0;    // O^T: dims 128 i .. as columns 64 i .. 64 i + 63
+constexpr uint32_t kSCol = 256;  // S^T: columns 256 .. 319
 constexpr unsigned long long kTimeoutNs = 500ull * 1000 * 1000;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLazy = 8.0f;                         // a head's reference maximum moves by more than this only
+constexpr float kLazy = 8.0f;    // a head's reference maximum moves by more than this only
+constexpr int kCodeWords = DS4X_KV_NOPE / 4;                      // 112 words of E4M3 codes
+constexpr int kRowWords = (DS4X_KV_NOPE + 2 * DS4X_KV_ROPE) / 4;  // 144 words of codes + RoPE
 
-// Shared-memory byte offsets of element (row, dim) of V' / (head, dim) of Q' /
-// (row, head) of P^T: core matrices of 8 x 8 fp16 values (16-byte rows).
-__device__ __forceinline__ uint32_t kv_off(int r, int chunk) { return uint32_t(r >> 3) * 8192u + uint32_t(chunk) * 128u + uint32_t(r & 7) * 16u; }
-__device__ __forceinline__ uint32_t q_off(int h, int chunk) { return uint32_t(h >> 3) * 8192u + uint32_t(chunk) * 128u + uint32_t(h & 7) * 16u; }
-__device__ __forceinline__ uint32_t p_off(int r, int hchunk) { return uint32_t(r >> 3) * 1024u + uint32_t(hchunk) * 128u + uint32_t(r & 7) * 16u; }
+// Byte offsets in the swizzled operands: V' (row r, 8-dim chunk C), Q' (head
+// h, chunk C), P^T (row r, 8-head chunk hc).  A panel holds 64 dims (heads)
+// of every row (head): 128 bytes a row, chunk c at position c ^ (row % 8).
+__device__ __forceinline__ uint32_t v_off(int r, int C) {
+  return uint32_t(C >> 3) * 16384u + uint32_t(r) * 128u + (uint32_t((C & 7) ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t q_off(int h, int C) {
+  return uint32_t(C >> 3) * 8192u + uint32_t(h) * 128u + (uint32_t((C & 7) ^ (h & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t p_off(int r, int hc) { return uint32_t(r) * 128u + (uint32_t(hc ^ (r & 7)) << 4); }
 
-struct __align__(128) ASmem {
-  uint8_t qs[kHeads * kDim * 2];   // Q' (B of the first MMA, K-major)
-  uint8_t kv[kTile * kDim * 2];    // V' (A of both MMAs)
-  uint8_t p_hi[kTile * kHeads * 2];  // P^T hi / lo (B of the second MMA, MN-major)
+// Shared-memory descriptor, 128-byte swizzle.  K-major: sbo = distance of
+// 8-row groups (a K step moves the start 32 bytes inside the panel).
+// MN-major: lbo = distance of 64-wide panels along M (N), sbo = distance of
+// 8-row groups along K.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+struct __align__(1024) ASmem {
+  uint8_t qs[kHeads * kDim * 2];     // Q' (B of the first MMA, K-major): 8 panels of 8 KB
+  uint8_t kv[kTile * kDim * 2];      // V' (A of both MMAs): 8 panels of 16 KB
+  uint8_t p_hi[kTile * kHeads * 2];  // P^T hi / lo (B of the second MMA, MN-major): one panel each
   uint8_t p_lo[kTile * kHeads * 2];
-  float red[2][4][kHeads];         // per-quadrant maxima / sums, double-buffered by use
-  float qscale[kHeads];            // scale * log2(e) * 2^-c_h
-  int sb[8];                       // S_b (UE8M0 bytes); sb[7] = 127 (RoPE)
-  uint8_t rvalid[kTile];           // the tile's row j is a selected, in-range row
+  float red[4][kHeads];              // per-quadrant maxima (each tile), then sums (each query)
+  float qscale[kHeads];              // scale * log2(e) * 2^-c_h
+  int sb[2][8];                      // S_b (UE8M0 bytes; [7] = 127 for the RoPE part), by query parity
+  uint8_t rvalid[kTile];             // the tile's row j is a selected, in-range row
   unsigned long long s_full, pv_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -142,12 +160,7 @@ __device__ __forceinline__ uint32_t pow2_half_bits(int e) {
   return 0u;
 }
 
-// Two E4M3 codes (bits 0-7 and 8-15) -> fp16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v));
-  return r;
-}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
 
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -186,9 +199,69 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   return r;
 }
 
+__device__ __forceinline__ bool row_ok(const PrefillAttnArgs &a, int32_t row) {
+  return row >= 0 && int64_t(row) < a.n_rows;
+}
+
+// The 8 rows of a warp's share of tile t (row k's index in lane 8 t + k of
+// `rows`): lane L loads each row's 4-byte aligned words L + 32 i, i < 5, up
+// to word 144 (which ends at row byte 580 at most, so every word read lies
+// inside its row).  A skipped row, or a tile past the last, reads nothing and
+// gives zeros.
+__device__ __forceinline__ void load_tile_words(const PrefillAttnArgs &a, int32_t rows, int t, int n_tiles, int lane,
+                                               uint32_t (&w)[8][5]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int32_t row = __shfl_sync(0xffffffffu, rows, (8 * t + k) & 31);
+    if (t < n_tiles && row_ok(a, row)) {  // warp-uniform
+      const int64_t o = int64_t(row) * DS4X_KV_ROW_BYTES;
+      const uint32_t *wp = reinterpret_cast<const uint32_t *>(a.kv + (o & ~int64_t(3)));
+#pragma unroll
+      for (int i = 0; i < 5; ++i) w[k][i] = 32 * i + lane <= kRowWords ? __ldg(wp + 32 * i + lane) : 0u;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 5; ++i) w[k][i] = 0u;
+    }
+  }
+}
+
+// Lane L's row of query qi: row 8 warp + L % 8 of tile L / 8 (-1 past k).
+__device__ __forceinline__ int32_t query_row(const PrefillAttnArgs &a, int qi, int warp, int lane) {
+  const int pos = kTile * (lane >> 3) + 8 * warp + (lane & 7);
+  return pos < a.k ? __ldg(a.idx + int64_t(qi) * a.k + pos) : -1;
+}
+
+// The row's 7 scale bytes (a skipped row reads row 0's, dropped by pack_scales).
+__device__ __forceinline__ void load_scale_bytes(const PrefillAttnArgs &a, int32_t row, uint32_t (&b)[kNopeBlocks]) {
+  const uint8_t *sp =
+      a.kv + (row_ok(a, row) ? int64_t(row) * DS4X_KV_ROW_BYTES : 0) + DS4X_KV_NOPE + 2 * DS4X_KV_ROPE;
+#pragma unroll
+  for (int i = 0; i < kNopeBlocks; ++i) b[i] = __ldg(sp + i);
+}
+// ... as scale bytes 0-3 / 4-6 (zeros for a skipped row).
+__device__ __forceinline__ void pack_scales(const PrefillAttnArgs &a, int32_t row, const uint32_t (&b)[kNopeBlocks],
+                                            uint32_t &sc0, uint32_t &sc1) {
+  const bool v = row_ok(a, row);
+  sc0 = v ? b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24) : 0u;
+  sc1 = v ? b[4] | (b[5] << 8) | (b[6] << 16) : 0u;
+}
+
+// This thread's 64 query values (head qh, block qb) of query qi, copied raw
+// (cp.async, 16 bytes a copy) to their Q' places; the thread waits for its
+// own copies before it converts them.
+__device__ __forceinline__ void copy_query_async(ASmem &sm, const PrefillAttnArgs &a, int qi, int qh, int qb) {
+  const uint16_t *src = a.q + (int64_t(qi) * kHeads + qh) * kDim + 64 * qb;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sm.qs + q_off(qh, 8 * qb + c))),
+                 "l"(src + 8 * c)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnArgs a, WsHeader *__restrict__ hdr) {
   extern __shared__ uint8_t smem_raw[];
-  ASmem &sm = *reinterpret_cast<ASmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  ASmem &sm = *reinterpret_cast<ASmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (a.k + kTile - 1) / kTile;
 
@@ -198,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     sm.abort_flag = 0;
     fence_mbar_init();
   }
+  if (tid < 16) sm.sb[tid >> 3][tid & 7] = (tid & 7) < kNopeBlocks ? 0 : 127;
   if (warp == 0) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -215,49 +289,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   const int qd = warp & 3, hg = warp >> 2;  // softmax: tile rows 32 qd + lane, heads 16 hg .. 16 hg + 15
   const int r_sm = 32 * qd + lane;
   const uint32_t lane_base = uint32_t(32 * qd) << 16;
+  // the row sums: after the butterfly each lane holds head hl of its warp's group
+  const int hl = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+  const int qh = tid >> 3, qb = tid & 7;  // Q': head tid / 8, block tid % 8
   uint32_t g = 0;   // tiles so far (the phase of s_full and pv_done)
-  int rp = 0;       // uses of red so far
-  int pending = 0;  // thread 0: 1 = s_full of tile g - 1 committed last, 2 = its pv_done
+  int pending = 0;  // thread 0: 1 = s_full of the current tile committed last, 2 = pv_done of the last tile
   bool ok = true, aborted = false;
-  for (int qi = blockIdx.x; qi < a.T && !aborted; qi += gridDim.x) {
+  int qn = 0;       // queries so far: sb[qn & 1] is this query's
+  // this query's inputs: lane L's row (row 8 warp + L % 8 of tile L / 8) and its
+  // scale bytes 0-3 / 4-6 (the raw query values are copied to Q''s places)
+  int32_t rowm = -1;
+  uint32_t sc0 = 0, sc1 = 0;
+  if (int(blockIdx.x) < a.T) {  // the first query's inputs (later queries' arrive during the previous epilogue)
+    copy_query_async(sm, a, blockIdx.x, qh, qb);
+    rowm = query_row(a, blockIdx.x, warp, lane);
+    uint32_t b[kNopeBlocks];
+    load_scale_bytes(a, rowm, b);
+    pack_scales(a, rowm, b, sc0, sc1);
+  }
+  for (int qi = blockIdx.x; qi < a.T && !aborted; qi += gridDim.x, ++qn) {
     const int32_t *idxq = a.idx + int64_t(qi) * a.k;
-    // ---- S_b: the largest scale byte of each non-RoPE block over the selected rows
-    if (named_bar_or(1, kThreads, !ok)) break;  // the previous query's readers of sb are done
-    if (tid < 8) sm.sb[tid] = tid < kNopeBlocks ? 0 : 127;
-    named_bar_sync(3, kThreads);
-    {
-      uint32_t sc[kNopeBlocks];
+    int *sbq = sm.sb[qn & 1];
+    if (named_bar_or(1, kThreads, !ok)) break;  // the previous query's readers of Q', sb[(qn + 1) & 1] are done
+    if (tid < 8) sm.sb[(qn + 1) & 1][tid] = tid < kNopeBlocks ? 0 : 127;  // for the next query
+    if (!row_ok(a, rowm) && rowm != -1) atomicExch(&hdr->status, int32_t(DS4X_EDEVICE));
 #pragma unroll
-      for (int b = 0; b < kNopeBlocks; ++b) sc[b] = 0;
-      if (tid < a.k) {
-        const int32_t row = idxq[tid];
-        if (row >= 0 && int64_t(row) < a.n_rows) {
-          const uint8_t *sp = a.kv + int64_t(row) * DS4X_KV_ROW_BYTES + DS4X_KV_NOPE + 2 * DS4X_KV_ROPE;
-#pragma unroll
-          for (int b = 0; b < kNopeBlocks; ++b) sc[b] = sp[b];
-        } else if (row != -1) {
-          atomicExch(&hdr->status, int32_t(DS4X_EDEVICE));
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kNopeBlocks; ++b) {
-        const uint32_t m = redux_max_u(sc[b]);
-        if (lane == 0 && m > 0) atomicMax(&sm.sb[b], int(m));
-      }
+    for (int b = 0; b < kNopeBlocks; ++b) {  // S_b
+      const uint32_t m = redux_max_u(((b < 4 ? sc0 >> (8 * b) : sc1 >> (8 * (b - 4)))) & 0xffu);
+      if (lane == 0 && m > 0) atomicMax(&sbq[b], int(m));
     }
     if (named_bar_or(1, kThreads, !ok)) break;
-    // ---- Q': thread (head tid / 8, block tid % 8) ----------------------------------
-    {
-      const int h = tid >> 3, b = tid & 7;
-      const int sh_b = sm.sb[b] - 127;
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (int64_t(qi) * kHeads + h) * kDim + 64 * b);
-      uint4 v[8];
+    uint32_t raw[8][5];  // the words of the warp's 8 rows of the next tile to widen (tile 0's
+    load_tile_words(a, rowm, 0, n_tiles, lane, raw);  // arrive while Q' is converted)
+    // the lane's row's fp16 factors 2^(s_b - S_b): blocks 2 i (low half) and 2 i + 1 of fac[i]
+    uint32_t fac[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) v[c] = src[c];
-      int emax = -1;  // largest bf16 exponent field among the normal values
+    for (int i = 0; i < 4; ++i) {
+      const int b0 = 2 * i, b1 = 2 * i + 1;
+      const uint32_t s_0 = (b0 < 4 ? sc0 >> (8 * b0) : sc1 >> (8 * (b0 - 4))) & 0xffu;
+      const uint32_t s_1 = b1 < kNopeBlocks ? (b1 < 4 ? sc0 >> (8 * b1) : sc1 >> (8 * (b1 - 4))) & 0xffu : 0u;
+      fac[i] = pow2_half_bits(int(s_0) - sbq[b0]) |
+               (b1 < kNopeBlocks ? pow2_half_bits(int(s_1) - sbq[b1]) << 16 : 0u);
+    }
+    // ---- Q' in place: this thread's 64 values times 2^(S_b - 127 + c_h), to fp16 ----------
+    {
+      asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's raw query values
+      uint4 qv[8];
+      int emax = -1;  // the largest bf16 exponent field among the normal values
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        qv[c] = *reinterpret_cast<const uint4 *>(sm.qs + q_off(qh, 8 * qb + c));
+        const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int e0 = int((w4[u] >> 7) & 0xff), e1 = int((w4[u] >> 23) & 0xff);
@@ -265,78 +347,73 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
           if (e1 != 0) emax = max(emax, e1);
         }
       }
+      const int sh_b = sbq[qb] - 127;
       int eh = emax < 0 ? -100000 : emax - 127 + sh_b;
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) eh = max(eh, __shfl_xor_sync(0xffffffffu, eh, o));
       const int c_h = eh == -100000 ? 0 : 14 - eh;
-      const int shift = sh_b + c_h;
+      // x * 2^(sh_b + c_h) as two exact power-of-two products (each factor a normal float)
+      const int s1 = max(-126, min(127, sh_b + c_h)), s2 = max(-126, min(127, sh_b + c_h - s1));
+      const float f1 = pow2f(s1), f2 = pow2f(s2);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        uint4 *qp = reinterpret_cast<uint4 *>(sm.qs + q_off(qh, 8 * qb + c));
+        const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
         uint32_t o4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float x0 = ldexpf(__uint_as_float(w4[u] << 16), shift);
-          const float x1 = ldexpf(__uint_as_float(w4[u] & 0xffff0000u), shift);
+          const float x0 = __uint_as_float(w4[u] << 16) * f1 * f2;
+          const float x1 = __uint_as_float(w4[u] & 0xffff0000u) * f1 * f2;
           const __half2 hv = __floats2half2_rn(x0, x1);
           o4[u] = *reinterpret_cast<const uint32_t *>(&hv);
         }
-        *reinterpret_cast<uint4 *>(sm.qs + q_off(h, 8 * b + c)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        *qp = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-      if (b == 0) sm.qscale[h] = ldexpf(a.scale * kLog2e, -c_h);
+      if (qb == 0) {
+        const int e1 = max(-126, min(127, -c_h)), e2 = max(-126, min(127, -c_h - e1));
+        sm.qscale[qh] = a.scale * kLog2e * pow2f(e1) * pow2f(e2);
+      }
     }
     fence_proxy_async_smem();
 
-    float m_ref[16], sums[16];
+    int32_t rowm_next = -1;  // the next query's rows (requested in the last tile)
+    float m_ref[16];  // head 16 hg + i's reference maximum (log2 units), the same in every lane
+    float m_lane = -INFINITY, wsum = 0.0f;  // head 16 hg + hl: the same maximum, the warp's rows' sum
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      m_ref[i] = -INFINITY;
-      sums[i] = 0.0f;
-    }
+    for (int i = 0; i < 16; ++i) m_ref[i] = -INFINITY;
     for (int t = 0; t < n_tiles; ++t, ++g) {
       // ---- widen tile t into V' (after the previous tile's second MMA) ----------
       if (g > 0 && !wait_bar(sm, &sm.pv_done, (g - 1) & 1, hdr)) ok = false;
-#pragma unroll 1
-      for (int ps = 0; ps < 2; ++ps) {
-        const int rr = 64 * ps + 8 * (warp >> 1) + (lane & 7);
-        const int j = 4 * (warp & 1) + (lane >> 3);
-        const int pos = kTile * t + rr;
-        const int32_t row = pos < a.k ? idxq[pos] : -1;
-        const bool valid = row >= 0 && int64_t(row) < a.n_rows;
-        if (j == 0) sm.rvalid[rr] = valid ? 1 : 0;
-        uint4 oc[8];
-        if (valid) {
-          const uint8_t *rowp = a.kv + int64_t(row) * DS4X_KV_ROW_BYTES;
-          const uint32_t o3 = uint32_t(reinterpret_cast<uintptr_t>(rowp)) & 3u;
-          const uint32_t *wn = reinterpret_cast<const uint32_t *>(rowp + 56 * j - o3);
-          const uint32_t *wr = reinterpret_cast<const uint32_t *>(rowp + DS4X_KV_NOPE + 16 * j - o3);
-          uint32_t raw[15], rw[5];
 #pragma unroll
-          for (int i = 0; i < 15; ++i) raw[i] = __ldg(wn + i);
+      for (int k = 0; k < 8; ++k) {
+        const int r = 8 * warp + k, src = 8 * t + k;
+        const int32_t row = __shfl_sync(0xffffffffu, rowm, src);
+        if (lane == 0) sm.rvalid[r] = row_ok(a, row) ? 1 : 0;
+        // a skipped row's words are zeros, so it widens to zeros with any shift and factor
+        const uint32_t sh = 8u * (uint32_t(row) * uint32_t(DS4X_KV_ROW_BYTES) & 3u);
+        uint32_t nx[5];  // word m + 1: from lane L + 1 (lane 31: lane 0's next stretch)
 #pragma unroll
-          for (int i = 0; i < 5; ++i) rw[i] = __ldg(wr + i);
-          const int blo = (7 * j) >> 3, bhi = (7 * j + 6) >> 3;
-          const uint8_t *scp = rowp + DS4X_KV_NOPE + 2 * DS4X_KV_ROPE;
-          const uint32_t flo = pow2_half_bits(int(__ldg(scp + blo)) - sm.sb[blo]) * 0x10001u;
-          const uint32_t fhi = pow2_half_bits(int(__ldg(scp + bhi)) - sm.sb[bhi]) * 0x10001u;
-          const uint32_t sh = 8u * o3;
+        for (int i = 0; i < 5; ++i) nx[i] = __shfl_sync(0xffffffffu, raw[k][i], (lane + 1) & 31);
 #pragma unroll
-          for (int i = 0; i < 7; ++i) {
-            const uint32_t f = ((7 * j + i) >> 3) == blo ? flo : fhi;
-            const uint32_t u0 = __funnelshift_r(raw[2 * i], raw[2 * i + 1], sh);
-            const uint32_t u1 = __funnelshift_r(raw[2 * i + 1], raw[2 * i + 2], sh);
-            oc[i] = make_uint4(hmul2_bits(e4m3x2_to_f16x2(u0 & 0xffffu), f), hmul2_bits(e4m3x2_to_f16x2(u0 >> 16), f),
-                               hmul2_bits(e4m3x2_to_f16x2(u1 & 0xffffu), f), hmul2_bits(e4m3x2_to_f16x2(u1 >> 16), f));
+        for (int i = 0; i < 5; ++i) {
+          const int m = 32 * i + lane;  // the row's 4-byte word m (bytes 4 m .. 4 m + 3)
+          const uint32_t wv = __funnelshift_r(raw[k][i], lane == 31 ? (i < 4 ? nx[i + 1] : 0u) : nx[i], sh);
+          // (every lane takes part in the shuffle, before the branch)
+          const uint32_t fw = i < 4 ? __shfl_sync(0xffffffffu, fac[i < 4 ? i : 0], src) : 0u;
+          if (i < 3 || (i == 3 && lane < 16)) {  // four E4M3 codes of block m / 16 = 2 i + lane / 16
+            const uint32_t f = ((lane & 16) ? fw >> 16 : fw & 0xffffu) * 0x10001u;
+            uint32_t h0, h1;
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+                : "=r"(h0), "=r"(h1)
+                : "r"(wv));
+            *reinterpret_cast<uint2 *>(sm.kv + v_off(r, m >> 1) + (m & 1) * 8) =
+                make_uint2(hmul2_bits(h0, f), hmul2_bits(h1, f));
+          } else if (i == 3 || lane < 16) {  // two FP16 RoPE values
+            const int rm = m - kCodeWords;
+            *reinterpret_cast<uint32_t *>(sm.kv + v_off(r, DS4X_KV_NOPE / 8 + (rm >> 2)) + (rm & 3) * 4) = wv;
           }
-          oc[7] = make_uint4(__funnelshift_r(rw[0], rw[1], sh), __funnelshift_r(rw[1], rw[2], sh),
-                             __funnelshift_r(rw[2], rw[3], sh), __funnelshift_r(rw[3], rw[4], sh));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) oc[i] = make_uint4(0u, 0u, 0u, 0u);
         }
-#pragma unroll
-        for (int i = 0; i < 7; ++i) *reinterpret_cast<uint4 *>(sm.kv + kv_off(rr, 7 * j + i)) = oc[i];
-        *reinterpret_cast<uint4 *>(sm.kv + kv_off(rr, 56 + j)) = oc[7];
       }
       fence_proxy_async_smem();
       if (named_bar_or(1, kThreads, !ok)) {  // every warp's V' (and Q', rvalid) written
@@ -347,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         tc_fence_after();
 #pragma unroll 4
         for (int ks = 0; ks < kDim / 16; ++ks)
-          mma_f16_ss(tmem + kSCol, smem_desc_noswizzle(kv_a + 256u * ks, 128, 8192),
-                     smem_desc_noswizzle(q_a + 256u * ks, 128, 8192), kIdS, ks > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + kSCol, desc_sw128(kv_a + 16384u * (ks >> 2) + 32u * (ks & 3), 16, 1024),
+                     desc_sw128(q_a + 8192u * (ks >> 2) + 32u * (ks & 3), 16, 1024), kIdS, ks > 0 ? 1u : 0u);
         tc_commit(smem_u32(&sm.s_full));
         pending = 1;
       }
@@ -356,15 +433,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
       // ---- softmax of tile t ------------------------------------------------------
       if (!wait_bar(sm, &sm.s_full, g & 1, hdr)) ok = false;
       tc_fence_after();
-      uint32_t sv[16];
-      tc_ld_x16(tmem + lane_base + kSCol + 16u * hg, sv);
-      tc_wait_ld();
-      const bool rv = sm.rvalid[r_sm] != 0;
       float l[16];
+      {
+        uint32_t sv[16];
+        tc_ld_x16(tmem + lane_base + kSCol + 16u * hg, sv);
+        tc_wait_ld();
+        const bool rv0 = sm.rvalid[r_sm] != 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) l[i] = rv ? __uint_as_float(sv[i]) * sm.qscale[16 * hg + i] : -INFINITY;
-      float *red = &sm.red[rp & 1][0][0];
-      ++rp;
+        for (int i = 0; i < 16; ++i) l[i] = rv0 ? __uint_as_float(sv[i]) * sm.qscale[16 * hg + i] : -INFINITY;
+      }
+      float *red = &sm.red[0][0];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int mx = redux_max(ordered_int(l[i]));
@@ -381,8 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         if (mt > m_ref[i] + kLazy) {
           alpha[i] = m_ref[i] == -INFINITY ? 0.0f : ex2(m_ref[i] - mt);
           m_ref[i] = mt;
-          sums[i] *= alpha[i];
           rescale = true;
+        }
+      }
+      {  // the same decision for this lane's head of the sum
+        const int hh = 16 * hg + hl;
+        const float mt = fmaxf(fmaxf(red[hh], red[kHeads + hh]), fmaxf(red[2 * kHeads + hh], red[3 * kHeads + hh]));
+        if (mt > m_lane + kLazy) {
+          wsum *= m_lane == -INFINITY ? 0.0f : ex2(m_lane - mt);
+          m_lane = mt;
         }
       }
       if (rescale && t > 0) {  // warp-uniform: every lane of a warp holds the same maxima
@@ -398,23 +483,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         }
         tc_wait_st();
       }
-      uint32_t ph[8], pl[8];
+      {
+        const bool rv = sm.rvalid[r_sm] != 0;
+        uint32_t ph[8], pl[8];
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const float p0 = rv ? ex2(l[i] - m_ref[i]) : 0.0f;
-        const float p1 = rv ? ex2(l[i + 1] - m_ref[i + 1]) : 0.0f;
-        sums[i] += p0;
-        sums[i + 1] += p1;
-        const __half2 hi = __floats2half2_rn(p0, p1);
-        const float2 hf = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
-        ph[i / 2] = *reinterpret_cast<const uint32_t *>(&hi);
-        pl[i / 2] = *reinterpret_cast<const uint32_t *>(&lo);
+        for (int i = 0; i < 16; i += 2) {
+          const float p0 = rv ? ex2(l[i] - m_ref[i]) : 0.0f;
+          const float p1 = rv ? ex2(l[i + 1] - m_ref[i + 1]) : 0.0f;
+          l[i] = p0;
+          l[i + 1] = p1;
+          const __half2 hi = __floats2half2_rn(p0, p1);
+          const float2 hf = __half22float2(hi);
+          const __half2 lo = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
+          ph[i / 2] = *reinterpret_cast<const uint32_t *>(&hi);
+          pl[i / 2] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
+        *reinterpret_cast<uint4 *>(sm.p_hi + p_off(r_sm, 2 * hg)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4 *>(sm.p_hi + p_off(r_sm, 2 * hg + 1)) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+        *reinterpret_cast<uint4 *>(sm.p_lo + p_off(r_sm, 2 * hg)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        *reinterpret_cast<uint4 *>(sm.p_lo + p_off(r_sm, 2 * hg + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
       }
-      *reinterpret_cast<uint4 *>(sm.p_hi + p_off(r_sm, 2 * hg)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-      *reinterpret_cast<uint4 *>(sm.p_hi + p_off(r_sm, 2 * hg + 1)) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-      *reinterpret_cast<uint4 *>(sm.p_lo + p_off(r_sm, 2 * hg)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-      *reinterpret_cast<uint4 *>(sm.p_lo + p_off(r_sm, 2 * hg + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
       fence_proxy_async_smem();
       tc_fence_before();
       if (named_bar_or(1, kThreads, !ok)) {  // every warp's P^T (and O^T rescale) written
@@ -427,14 +515,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         for (int mi = 0; mi < kDim / 128; ++mi) {
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint64_t ad = smem_desc_noswizzle(kv_a + 2048u * mi + 16384u * ks, 8192, 128);
-            mma_f16_ss(tmem + kOCol + 64u * mi, ad, smem_desc_noswizzle(ph_a + 2048u * ks, 1024, 128), kIdO,
+            const uint64_t ad = desc_sw128(kv_a + 32768u * mi + 2048u * ks, 16384, 1024);
+            mma_f16_ss(tmem + kOCol + 64u * mi, ad, desc_sw128(ph_a + 2048u * ks, 8192, 1024), kIdO,
                        (t > 0 || ks > 0) ? 1u : 0u);
-            mma_f16_ss(tmem + kOCol + 64u * mi, ad, smem_desc_noswizzle(pl_a + 2048u * ks, 1024, 128), kIdO, 1u);
+            mma_f16_ss(tmem + kOCol + 64u * mi, ad, desc_sw128(pl_a + 2048u * ks, 8192, 1024), kIdO, 1u);
           }
         }
         tc_commit(smem_u32(&sm.pv_done));
         pending = 2;
+      }
+      // the next tile's words arrive while this tile's second MMA runs (requested
+      // after the proxy fence above, which would otherwise wait for them)
+      load_tile_words(a, rowm, t + 1, n_tiles, lane, raw);
+      if (t + 1 == n_tiles) rowm_next = qi + int(gridDim.x) < a.T ? query_row(a, qi + int(gridDim.x), warp, lane) : -1;
+      // this tile's p summed over the warp's 32 rows, head by head (a butterfly:
+      // after it lane L holds head hl(L)), added to the lane's running sum
+      {
+        float w8[8], w4[4], w2[2];
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float send = b4 ? l[k] : l[k + 8], keep = b4 ? l[k + 8] : l[k];
+          w8[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float send = b3 ? w8[k] : w8[k + 4], keep = b3 ? w8[k + 4] : w8[k];
+          w4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float send = b2 ? w4[k] : w4[k + 2], keep = b2 ? w4[k + 2] : w4[k];
+          w2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        const float send = b1 ? w2[0] : w2[1], keep = b1 ? w2[1] : w2[0];
+        float w1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+        wsum += w1;
       }
     }
     if (aborted) break;
@@ -442,15 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     // ---- the query's output: O^T / sum, block scales put back ---------------------------
     if (!wait_bar(sm, &sm.pv_done, (g - 1) & 1, hdr)) ok = false;
     tc_fence_after();
-    float *red = &sm.red[rp & 1][0][0];
-    ++rp;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s = sums[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == i) red[qd * kHeads + 16 * hg + i] = s;
-    }
+    // the next query's scale bytes and values are requested now and used after the output
+    const bool more = qi + int(gridDim.x) < a.T;
+    uint32_t scb_next[kNopeBlocks];  // packed after the output (their loads are in flight meanwhile)
+    load_scale_bytes(a, rowm_next, scb_next);
+    if (more) copy_query_async(sm, a, qi + int(gridDim.x), qh, qb);  // Q''s buffer is free: the last first MMA is done
+    float *red = &sm.red[0][0];
+    if ((lane & 1) == 0) red[qd * kHeads + 16 * hg + hl] = wsum;
     if (named_bar_or(1, kThreads, !ok)) break;
     float inv[16];
 #pragma unroll
@@ -461,19 +576,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
       if (a.lse != nullptr && qd == 0 && lane == i)
         a.lse[int64_t(qi) * kHeads + hh] = tot > 0.0f ? (m_ref[i] + log2f(tot)) * 0.6931471805599453f : -INFINITY;
     }
-    uint16_t *outq = a.out + int64_t(qi) * kHeads * kDim;
+    // o as bf16 [head][dim] in V''s space (free once the last second MMA is done),
+    // then out with 16-byte stores
+    uint16_t *os = reinterpret_cast<uint16_t *>(sm.kv);
 #pragma unroll 1
     for (int mi = 0; mi < kDim / 128; ++mi) {
       uint32_t ov[16];
       tc_ld_x16(tmem + lane_base + kOCol + 64u * mi + 16u * hg, ov);
       tc_wait_ld();
       const int d = 128 * mi + 32 * qd + lane;
-      const float fb = ldexpf(1.0f, sm.sb[d >> 6] - 127);
+      const float fb = ldexpf(1.0f, sbq[d >> 6] - 127);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        outq[(16 * hg + i) * kDim + d] = f32_to_bf16_rn((__uint_as_float(ov[i]) * inv[i]) * fb);
+        os[(16 * hg + i) * kDim + d] = f32_to_bf16_rn((__uint_as_float(ov[i]) * inv[i]) * fb);
     }
     tc_fence_before();
+    named_bar_sync(2, kThreads);
+    {
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(sm.kv);
+      uint4 *o4 = reinterpret_cast<uint4 *>(a.out + int64_t(qi) * kHeads * kDim);
+#pragma unroll
+      for (int c = 0; c < kHeads * kDim * 2 / 16 / kThreads; ++c) o4[tid + c * kThreads] = s4[tid + c * kThreads];
+    }
+    pack_scales(a, rowm_next, scb_next, sc0, sc1);
+    rowm = rowm_next;
   }
   if (aborted || !ok) {  // thread 0: no MMA may still write this CTA's memory when it exits
     if (tid == 0 && pending == 1) drain_bar(&sm.s_full, (g - 1 + (aborted ? 1 : 0)) & 1);
@@ -496,7 +622,8 @@ cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const in
                                 int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
                                 cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
-  const int smem = int(sizeof(ASmem)) + 128;
+  // the dynamic shared memory is at least 16-byte aligned: room to round it up to 1024
+  const int smem = int(sizeof(ASmem)) + 1024 - 16;
   cudaError_t e = set_max_smem_once(attn_prefill_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
