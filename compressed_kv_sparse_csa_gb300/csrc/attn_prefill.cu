@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   const uint32_t ph_a = smem_u32(sm.p_hi), pl_a = smem_u32(sm.p_lo);
   constexpr uint32_t kIdS = idesc_f16(128, kHeads, 0, 0);  // V' K-major, Q' K-major
   constexpr uint32_t kIdO = idesc_f16(128, kHeads, 1, 1);  // V'^T MN-major, P^T MN-major
+  // the operands' descriptors at their first K step (later steps add to the address field)
+  const uint64_t dS_a = desc_sw128(kv_a, 16, 1024), dS_b = desc_sw128(q_a, 16, 1024);
+  const uint64_t dO_a = desc_sw128(kv_a, 16384, 1024);
+  const uint64_t dO_bh = desc_sw128(ph_a, 8192, 1024), dO_bl = desc_sw128(pl_a, 8192, 1024);
 
   const int qd = warp & 3, hg = warp >> 2;  // softmax: tile rows 32 qd + lane, heads 16 hg .. 16 hg + 15
   const int r_sm = 32 * qd + lane;
@@ -422,10 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
       }
       if (tid == 0) {
         tc_fence_after();
-#pragma unroll 4
+        // K step ks: 32 bytes into panel ks / 4 (the descriptors' address field counts 16 bytes)
+#pragma unroll
         for (int ks = 0; ks < kDim / 16; ++ks)
-          mma_f16_ss(tmem + kSCol, desc_sw128(kv_a + 16384u * (ks >> 2) + 32u * (ks & 3), 16, 1024),
-                     desc_sw128(q_a + 8192u * (ks >> 2) + 32u * (ks & 3), 16, 1024), kIdS, ks > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + kSCol, dS_a + uint64_t(1024 * (ks >> 2) + 2 * (ks & 3)),
+                     dS_b + uint64_t(512 * (ks >> 2) + 2 * (ks & 3)), kIdS, ks > 0 ? 1u : 0u);
         tc_commit(smem_u32(&sm.s_full));
         pending = 1;
       }
@@ -511,14 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
       }
       if (tid == 0) {
         tc_fence_after();
-#pragma unroll 1
-        for (int mi = 0; mi < kDim / 128; ++mi) {
+        // M tile mi: panels 2 mi, 2 mi + 1 (32 KB on); K step ks: 16 rows (2 KB) on.  The four
+        // M tiles' accumulators are independent: their MMAs interleave
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint64_t ad = desc_sw128(kv_a + 32768u * mi + 2048u * ks, 16384, 1024);
-            mma_f16_ss(tmem + kOCol + 64u * mi, ad, desc_sw128(ph_a + 2048u * ks, 8192, 1024), kIdO,
-                       (t > 0 || ks > 0) ? 1u : 0u);
-            mma_f16_ss(tmem + kOCol + 64u * mi, ad, desc_sw128(pl_a + 2048u * ks, 8192, 1024), kIdO, 1u);
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+#pragma unroll
+          for (int mi = 0; mi < kDim / 128; ++mi) {
+            const uint64_t ad = dO_a + uint64_t(2048 * mi + 128 * ks);
+            mma_f16_ss(tmem + kOCol + 64u * mi, ad, dO_bh + uint64_t(128 * ks), kIdO, ks > 0 ? 1u : acc0);
+            mma_f16_ss(tmem + kOCol + 64u * mi, ad, dO_bl + uint64_t(128 * ks), kIdO, 1u);
           }
         }
         tc_commit(smem_u32(&sm.pv_done));
