@@ -1,8 +1,8 @@
 """Benchmark of the compressed-KV sparse-attention decode step on GB300.
 
-One step = CSA indexer score + exact top-512 over all N compressed rows of
-one layer, then sparse attention of the 64-head decode query over the 512
-selected packed KV rows (batch 1).  Default workload: the long decode layer,
+One step = one ds4x_csa_decode_step call: CSA indexer score + exact top-512
+over all N compressed rows of one layer, then sparse attention of the
+64-head decode query over the 512 selected packed KV rows (batch 1).  Default workload: the long decode layer,
 N = 1,048,576 rows (68-byte MXFP4 indexer rows, 583-byte KV rows, 64 indexer
 heads x 128, 64 attention heads x 512), synthetic N(0,1) data packed by the
 library's own cache writer.

@@ -330,7 +330,14 @@ int ds4x_index_score_topk_prefill(const uint8_t *idx_rows, int64_t n_rows, const
  * Prefill sparse attention: each of n_queries query tokens attends over its
  * own k selected rows of one packed KV cache (DS4X README, "Packed prefill
  * implementation": per-token sparse attention after the batched score/top-k).
- * Per query exactly ds4x_sparse_attn_decode.
+ * Per query the attention of ds4x_sparse_attn_decode (the same skip and
+ * DS4X_EDEVICE rules, zeros and -inf for a query with no valid row), computed
+ * with tcgen05 fp16 products over 128-row tiles: each non-RoPE value enters as
+ * fp16 relative to the largest scale of its block over the query's rows, so
+ * it is exact while the query's rows' scales of a block lie within 2^15 of
+ * each other (beyond, a value rounds at 2^-24 of that block's largest scale);
+ * the query enters exactly, the softmax weights with 22 significant bits, sums
+ * in fp32.  One persistent CTA per SM takes the queries in turn.
  *
  *   kv_rows    u8 [n_rows][583]
  *   idx        i32 [n_queries][k]
