@@ -466,8 +466,9 @@ def main():
     # ---- end to end through the public API, host buffers, copies inside.
     # A step's inputs (the new row's 512 + 128 values, both queries, the head
     # weights) sit in one pinned block and cross in one copy; the attention
-    # output and the indices come back in one copy.  The public calls of a
-    # step (copy in, append, score, attend, copy out) are captured once per
+    # output and the indices come back in one copy (both ds4x_copy_async: a
+    # kernel reading / writing the pinned host block).  The public calls of a
+    # step (copy in, append, score + attend, copy out) are captured once per
     # layer as a CUDA graph, as a decode server would run them.
     e2e_steps = min(args.steps, 500)
     seg = [("kv", 512 * 4), ("idx", 128 * 4), ("q", HEADS * 128 * 2), ("w", HEADS * 4), ("qa", HEADS * 512 * 2)]
@@ -500,11 +501,11 @@ def main():
 
     def e2e_calls(l):
         c = layers[l]
-        d_in.copy_(h_in, non_blocking=True)
+        B.ds4x_copy_async(d_in, h_in, stream=stream)  # pinned host -> device, a kernel (no copy-engine hand-over)
         B.ds4x_cache_append(c["kv_rows"], c["idx_rows"], n - 1, d_kv, d_idx, stream=stream)
         B.ds4x_csa_decode_step(c["idx_rows"], c["kv_rows"], n, d_q, d_w, K_TOP, d_qa, scale, d_oidx, c["out_score"],
                                d_out, None, ws_d, stream=stream)
-        h_res.copy_(d_res, non_blocking=True)
+        B.ds4x_copy_async(h_res, d_res, stream=stream)  # device -> pinned host
 
     with torch.cuda.stream(stream):
         for l in range(L):
@@ -579,9 +580,9 @@ def main():
         "e2e": {"value": job_value(world, n, ms_e2e_step), "unit": "compressed rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": ms_e2e_step,
-                "path": "per step one CUDA graph of the public calls: one pinned-host-to-device copy of the "
-                        "packed inputs, ds4x_cache_append, ds4x_csa_decode_step (score + top-512, attention), one "
-                        "device-to-pinned-host copy of the output and indices"},
+                "path": "per step one CUDA graph of the public calls: ds4x_copy_async of the packed inputs from "
+                        "pinned host memory (a kernel), ds4x_cache_append, ds4x_csa_decode_step (score + top-512, "
+                        "attention), ds4x_copy_async of the output and indices to pinned host memory"},
         "gpu_launches": args.steps * (launches_per_step["score"] + launches_per_step["attn"]),
         "clocks": clocks,
     }

@@ -29,6 +29,7 @@ _SIGNATURES = {
     "ds4x_abi_version": (ctypes.c_int, []),
     "ds4x_cache_bytes": (_c_i64, [_c_i64]),
     "ds4x_workspace_init": (ctypes.c_int, [_c_p, _c_size, _c_p]),
+    "ds4x_copy_async": (ctypes.c_int, [_c_p, _c_p, _c_size, _c_p]),
     "ds4x_workspace_status": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(_c_i32)]),
     "ds4x_cache_append": (ctypes.c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_p]),
     "ds4x_index_score_topk_workspace": (_c_size, [_c_i64, _c_i32]),
@@ -129,6 +130,20 @@ def ds4x_cache_bytes(context_tokens: int) -> int:
 def ds4x_workspace_init(ws, stream=None):
     _check(ws, torch.uint8, "ws")
     _call("ds4x_workspace_init", _ptr(ws), ws.numel(), _stream(stream))
+
+
+def ds4x_copy_async(dst, src, stream=None):
+    """Kernel-side copy of src's bytes into dst (each a contiguous CUDA tensor
+    or a pinned host tensor; same number of bytes)."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _call("ds4x_copy_async", _ptr(dst), _ptr(src), nbytes, _stream(stream))
 
 
 def ds4x_workspace_status(ws, stream=None) -> int:

@@ -82,6 +82,16 @@ int ds4x_workspace_init(void *ws, size_t ws_bytes, ds4x_stream_t stream) {
   return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, stream));
 }
 
+int ds4x_copy_async(void *dst, const void *src, size_t bytes, ds4x_stream_t stream) {
+  if (dst == nullptr || src == nullptr || !aligned16(dst) || !aligned16(src)) return DS4X_EINVAL;
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+  if (bytes > 0 && d < s + bytes && s < d + bytes) return DS4X_EINVAL;  // overlapping
+  if (bytes == 0) return DS4X_OK;
+  const int a = check_arch();
+  if (a != DS4X_OK) return a;
+  return from_cuda(launch_copy(dst, src, bytes, stream));
+}
+
 int ds4x_workspace_status(void *ws, ds4x_stream_t stream, int32_t *status_host) {
   if (ws == nullptr || status_host == nullptr || !aligned16(ws)) return DS4X_EINVAL;
   const int a = check_arch();

@@ -176,6 +176,8 @@ size_t attn_prefill_ws_bytes();
 cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
                                 int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
                                 cudaStream_t stream);
+// Kernel-side copy (device or GPU-addressable pinned host memory on either side).
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,
                                int32_t k, const uint16_t *q, float scale, uint16_t *out,
                                float *lse, void *ws, cudaStream_t stream);

@@ -117,6 +117,20 @@ int64_t ds4x_cache_bytes(int64_t context_tokens);
 int ds4x_workspace_init(void *ws, size_t ws_bytes, ds4x_stream_t stream);
 
 /*
+ * Copies `bytes` bytes from src to dst with a kernel on `stream` (16-byte
+ * words, the tail byte by byte).  Either pointer may be device memory or
+ * page-locked host memory the GPU can address (cudaHostAlloc / pinned
+ * memory under unified addressing): a decode loop that keeps a step's inputs
+ * and results in pinned host memory moves them with this call inside its
+ * CUDA graph, instead of copy-engine copies whose hand-over to and from the
+ * kernels costs several microseconds each.  The pages have no counterpart
+ * to it.  dst and src 16-byte aligned and not overlapping; bytes may be 0
+ * (nothing is launched).  Asynchronous; the caller keeps both buffers alive
+ * until the stream has passed the copy.  Errors: DS4X_EINVAL.
+ */
+int ds4x_copy_async(void *dst, const void *src, size_t bytes, ds4x_stream_t stream);
+
+/*
  * Reads the device status word at the head of a workspace (a blocking copy
  * after synchronising `stream`) into *status_host and clears it.  It is
  * DS4X_OK, or DS4X_EDEVICE when an attention call met an index outside

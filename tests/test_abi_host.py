@@ -91,6 +91,16 @@ def test_attention_argument_checks(lib):
     assert f(FAKE, 10, FAKE, 512, FAKE, s, FAKE, None, FAKE, ws - 1, None) == -3
 
 
+def test_copy_argument_checks(lib):
+    f = lib.ds4x_copy_async
+    assert f(None, FAKE, 64, None) == -1
+    assert f(FAKE, None, 64, None) == -1
+    assert f(FAKE + 4, FAKE + 4096, 64, None) == -1  # misaligned
+    assert f(FAKE, FAKE + 32, 64, None) == -1        # overlapping
+    assert f(FAKE + 32, FAKE, 64, None) == -1
+    assert f(FAKE, FAKE + 4096, 0, None) == 0        # nothing to copy: no CUDA call
+
+
 def test_workspace_calls_reject_null(lib):
     assert lib.ds4x_workspace_init(None, 4096, None) == -1
     assert lib.ds4x_workspace_init(FAKE, 16, None) == -1
