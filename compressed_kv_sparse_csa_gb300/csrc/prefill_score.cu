@@ -388,7 +388,7 @@ struct __align__(16) TSmem {
   int bstar, above, bcnt, n_above, n_list;
 };
 
-__global__ void __launch_bounds__(kSelThreads) prefill_topk_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) prefill_topk_kernel(PrefillArgs a) {
   extern __shared__ uint8_t tsm_raw[];
   TSmem &sm = *reinterpret_cast<TSmem *>((reinterpret_cast<uintptr_t>(tsm_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
