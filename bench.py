@@ -716,7 +716,7 @@ def run_hca(args):
     """Dense decode attention over every compressed row of a ratio-128 (HCA)
     layer at a 1M-token context: 8192 rows of 583 B, 64 heads; 40 layer
     copies (191 MB, above the 129 MB L2) rotated, one CUDA graph per layer
-    (the 512-row tiles' attention and the finalize)."""
+    (the tensor-core attention over 64 items of 128 rows, then the combine)."""
     torch, B, dev, stream = _gpu_setup()
     n, L = 8192, 40
     gen = torch.Generator(device=dev)

@@ -178,10 +178,9 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
   return v;
 }
 
-// DENSE: item b is the tile of rows [512 b, 512 b + 512) (no index list),
-// every item reads the one query, and the normalised output goes to out_f32
-// in fp32 for the finalize.
-template <int HG, bool DENSE>
+// With ab.out_f32 set, item b's normalised output goes there in fp32 (for a
+// finalize) instead of to ab.out.
+template <int HG>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
 attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   using C = Cfg<HG>;
@@ -192,10 +191,10 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   const int64_t n_rows = ab.n_arr != nullptr ? ab.n_arr[bz] : ab.n_rows;
   const int k = ab.k;
   const float scale = ab.scale;
-  const int32_t *__restrict__ idx = DENSE ? nullptr : ab.idx + size_t(bz) * k;
+  const int32_t *__restrict__ idx = ab.idx + size_t(bz) * k;
   const uint16_t *__restrict__ q = ab.q + (ab.q_shared ? size_t(0) : size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM);
-  // fp32 output (dense tiles, window + sparse items) for a finalize, else bf16
-  const bool f32_out = DENSE || ab.out_f32 != nullptr;
+  // fp32 output (window + sparse items) for a finalize, else bf16
+  const bool f32_out = ab.out_f32 != nullptr;
   uint16_t *__restrict__ out = f32_out ? nullptr : ab.out + size_t(bz) * DS4X_ATTN_HEADS * DS4X_KV_DIM;
   float *__restrict__ lse = ab.lse != nullptr ? ab.lse + size_t(bz) * DS4X_ATTN_HEADS : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -235,10 +234,7 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
   if (tid < kRows) {
     const int j = split * kRows + tid;
     int64_t r = -1;
-    if (DENSE) {
-      const int64_t t = int64_t(bz) * DS4X_TOPK_MAX + j;  // the tile's rows
-      r = t < n_rows ? t : -1;
-    } else if (j < k) {
+    if (j < k) {
       r = idx[j];
       if (r < -1 || r >= n_rows) {
         atomicExch(&hdr->status, int32_t(DS4X_EDEVICE));
@@ -604,11 +600,11 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
 
 size_t attn_decode_ws_bytes(int32_t) { return kWsHeaderBytes; }
 
-template <int HG, bool DENSE = false>
+template <int HG>
 cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
   using C = Cfg<HG>;
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = set_max_smem_once(attn_decode_kernel<HG, DENSE>, int(C::kSmemBytes), smem_set);
+  cudaError_t e = set_max_smem_once(attn_decode_kernel<HG>, int(C::kSmemBytes), smem_set);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the CTAs may start while the previous
   // kernel finishes (it lets them go from its tail); the kernel waits for it
@@ -623,11 +619,10 @@ cudaError_t launch_attn_hg(const AttnBatch &ab, int batch, void *ws, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<HG, DENSE>, ab, static_cast<WsHeader *>(ws));
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<HG>, ab, static_cast<WsHeader *>(ws));
 }
 
-template <bool DENSE>
-cudaError_t launch_attn_items(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
+cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
   // the fewest heads per cluster whose grid fits one wave (two CTAs per SM):
   // the most CTAs, the shortest latency; beyond that 16, a quarter of the
   // CTAs of 4 heads for about twice the MMAs each (no zero rows)
@@ -636,53 +631,63 @@ cudaError_t launch_attn_items(const AttnBatch &ab, int batch, void *ws, cudaStre
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t wave = 2 * int64_t(sms);
-  if (int64_t(batch) * kCluster * Cfg<4>::kGroups <= wave) return launch_attn_hg<4, DENSE>(ab, batch, ws, stream);
-  if (int64_t(batch) * kCluster * Cfg<8>::kGroups <= wave) return launch_attn_hg<8, DENSE>(ab, batch, ws, stream);
-  return launch_attn_hg<16, DENSE>(ab, batch, ws, stream);
-}
-
-cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream) {
-  return launch_attn_items<false>(ab, batch, ws, stream);
+  if (int64_t(batch) * kCluster * Cfg<4>::kGroups <= wave) return launch_attn_hg<4>(ab, batch, ws, stream);
+  if (int64_t(batch) * kCluster * Cfg<8>::kGroups <= wave) return launch_attn_hg<8>(ab, batch, ws, stream);
+  return launch_attn_hg<16>(ab, batch, ws, stream);
 }
 
 namespace {
 
-// The dense attention's workspace: the status header, then per 512-row tile
-// t the LSEs [t][64] and the normalised outputs [t][64][512], fp32.
+// The dense attention's workspace: the status header, then per item i the
+// LSEs [i][64] and the normalised outputs [i][64][512], fp32.
 struct DenseWsLayout {
+  int32_t rows_per_item, items;
   size_t lse, o, total;
 };
 DenseWsLayout dense_layout(int64_t n_rows) {
-  const int64_t tiles = (n_rows + DS4X_TOPK_MAX - 1) / DS4X_TOPK_MAX;
   DenseWsLayout L{};
+  L.rows_per_item = dense_rows_per_item(n_rows);
+  L.items = int32_t((n_rows + L.rows_per_item - 1) / L.rows_per_item);
   L.lse = kWsHeaderBytes;
-  L.o = L.lse + ((size_t(tiles) * DS4X_ATTN_HEADS * sizeof(float) + 255) / 256) * 256;
-  L.total = L.o + size_t(tiles) * DS4X_ATTN_HEADS * DS4X_KV_DIM * sizeof(float);
+  L.o = L.lse + ((size_t(L.items) * DS4X_ATTN_HEADS * sizeof(float) + 255) / 256) * 256;
+  L.total = L.o + size_t(L.items) * DS4X_ATTN_HEADS * DS4X_KV_DIM * sizeof(float);
   return L;
 }
 
-// The split-KV combine over the tiles, one head per block: with M the largest
-// tile LSE, o = sum_t e^(lse_t - M) o_t / sum_t e^(lse_t - M) (o_t each tile's
-// normalised output), lse = M + log sum_t e^(lse_t - M).  Tile weights in
-// shared memory (T floats).
-__global__ void __launch_bounds__(256) dense_finalize_kernel(const float *__restrict__ lse_part,
-                                                             const float *__restrict__ o_part, int T,
-                                                             uint16_t *__restrict__ out, float *__restrict__ lse) {
+constexpr int kFinDims = 128;                      // output dims per block
+constexpr int kFinParts = 4;                       // item groups per block
+constexpr int kFinThreads = kFinDims * kFinParts;  // 512
+constexpr int kFinSplit = DS4X_KV_DIM / kFinDims;  // blocks per head
+
+// The split-KV combine over T items, block (h, c): head h, dims 128 c ..
+// 128 c + 127.  With M the largest item LSE, o = sum_t e^(lse_t - M) o_t /
+// sum_t e^(lse_t - M) (o_t each item's normalised output), lse = M + log sum_t
+// e^(lse_t - M).  Thread (p, d) sums items p, p + 4, ... of dim d (eight loads
+// in flight), the four sums are added in a fixed order.  Item weights in
+// shared memory (T floats).  Launched as a programmatic dependent of the
+// items' attention: it waits for it first.
+__global__ void __launch_bounds__(kFinThreads) dense_finalize_kernel(const float *__restrict__ lse_part,
+                                                                     const float *__restrict__ o_part, int T,
+                                                                     uint16_t *__restrict__ out,
+                                                                     float *__restrict__ lse) {
   extern __shared__ float fsh[];  // [T]: e^(lse_t - M)
-  __shared__ float red[8];
+  __shared__ float red[kFinThreads / 32];
+  __shared__ float osum[kFinParts][kFinDims];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kFinThreads / 32;
   float m = -INFINITY;
-  for (int t = tid; t < T; t += 256) m = fmaxf(m, lse_part[size_t(t) * DS4X_ATTN_HEADS + h]);
+  for (int t = tid; t < T; t += kFinThreads) m = fmaxf(m, lse_part[size_t(t) * DS4X_ATTN_HEADS + h]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) red[warp] = m;
   __syncthreads();
   float M = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
   __syncthreads();  // red is reused below
   float sum = 0.f;
-  for (int t = tid; t < T; t += 256) {
+  for (int t = tid; t < T; t += kFinThreads) {
     const float l = lse_part[size_t(t) * DS4X_ATTN_HEADS + h];
     const float f = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
     fsh[t] = f;
@@ -694,16 +699,51 @@ __global__ void __launch_bounds__(256) dense_finalize_kernel(const float *__rest
   __syncthreads();
   float L = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) L += red[w];
-  for (int d = tid; d < DS4X_KV_DIM; d += 256) {
-    float o = 0.f;
-    for (int t = 0; t < T; ++t) o = fmaf(fsh[t], o_part[(size_t(t) * DS4X_ATTN_HEADS + h) * DS4X_KV_DIM + d], o);
-    out[size_t(h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? o / L : 0.f));
+  for (int w = 0; w < kWarps; ++w) L += red[w];
+  const int dd = tid % kFinDims, part = tid / kFinDims;
+  const int d = kFinDims * blockIdx.y + dd;
+  const float *op = o_part + size_t(h) * DS4X_KV_DIM + d;
+  constexpr size_t kItem = size_t(DS4X_ATTN_HEADS) * DS4X_KV_DIM;  // floats between items
+  float o = 0.f;
+  int t = part;
+  for (; t + 7 * kFinParts < T; t += 8 * kFinParts) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = op[size_t(t + u * kFinParts) * kItem];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o = fmaf(fsh[t + u * kFinParts], v[u], o);
   }
-  if (tid == 0 && lse != nullptr) lse[h] = L > 0.f ? M + logf(L) : -INFINITY;
+  for (; t < T; t += kFinParts) o = fmaf(fsh[t], op[size_t(t) * kItem], o);
+  osum[part][dd] = o;
+  __syncthreads();
+  if (part == 0) {
+    const float tot = (osum[0][dd] + osum[1][dd]) + (osum[2][dd] + osum[3][dd]);
+    out[size_t(h) * DS4X_KV_DIM + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? tot / L : 0.f));
+  }
+  if (blockIdx.y == 0 && tid == 0 && lse != nullptr) lse[h] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+cudaError_t launch_finalize(const float *lse_part, const float *o_part, int T, uint16_t *out, float *lse,
+                            cudaStream_t stream) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(DS4X_ATTN_HEADS, kFinSplit);
+  cfg.blockDim = dim3(kFinThreads);
+  cfg.dynamicSmemBytes = size_t(T) * sizeof(float);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dense_finalize_kernel, lse_part, o_part, T, out, lse);
 }
 
 }  // namespace
+
+int32_t dense_rows_per_item(int64_t n_rows) {
+  const int64_t per = (n_rows + 128 * 256 - 1) / (128 * 256);  // 128-row tiles per item
+  return int32_t(128 * (per < 1 ? 1 : (per > 4 ? 4 : per)));
+}
 
 size_t dense_attn_ws_bytes(int64_t n_rows) { return dense_layout(n_rows < 1 ? 1 : n_rows).total; }
 
@@ -772,34 +812,22 @@ cudaError_t launch_window_attn(const uint8_t *kv_rows, int64_t n_rows, const int
   ab.q_shared = true;
   ab.lse = lse_part;
   ab.out_f32 = o_part;
-  e = launch_attn_items<false>(ab, 2, ws, stream);
+  e = launch_attn_batch(ab, 2, ws, stream);
   if (e != cudaSuccess) return e;
-  dense_finalize_kernel<<<DS4X_ATTN_HEADS, 256, 2 * sizeof(float), stream>>>(lse_part, o_part, 2, out, lse);
-  return cudaGetLastError();
+  return launch_finalize(lse_part, o_part, 2, out, lse, stream);
 }
 
 cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
                               float *lse, void *ws, cudaStream_t stream) {
-  const int64_t tiles = (n_rows + DS4X_TOPK_MAX - 1) / DS4X_TOPK_MAX;
-  if (n_rows < 1 || tiles > kDenseMaxTiles) return cudaErrorInvalidValue;
+  if (n_rows < 1 || n_rows > kDenseMaxTiles * DS4X_TOPK_MAX) return cudaErrorInvalidValue;
   const DenseWsLayout L = dense_layout(n_rows);
   char *base = static_cast<char *>(ws);
   float *lse_part = reinterpret_cast<float *>(base + L.lse);
   float *o_part = reinterpret_cast<float *>(base + L.o);
-  AttnBatch ab{};
-  ab.kv = kv_rows;
-  ab.n_rows = n_rows;
-  ab.k = DS4X_TOPK_MAX;
-  ab.scale = scale;
-  ab.q = q;
-  ab.q_shared = true;
-  ab.lse = lse_part;
-  ab.out_f32 = o_part;
-  cudaError_t e = launch_attn_items<true>(ab, int(tiles), ws, stream);
+  cudaError_t e = launch_attn_dense_items(kv_rows, n_rows, L.rows_per_item, L.items, q, scale, o_part, lse_part, ws,
+                                          stream);
   if (e != cudaSuccess) return e;
-  dense_finalize_kernel<<<DS4X_ATTN_HEADS, 256, size_t(tiles) * sizeof(float), stream>>>(lse_part, o_part, int(tiles),
-                                                                                         out, lse);
-  return cudaGetLastError();
+  return launch_finalize(lse_part, o_part, L.items, out, lse, stream);
 }
 
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

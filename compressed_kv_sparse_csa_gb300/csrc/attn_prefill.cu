@@ -8,6 +8,12 @@
 //   l_hj = scale * (q_h . v_j),  o_h = sum_j softmax_j(l_h)_j v_j,
 //   lse_h = log sum_j e^(l_hj)
 //
+// The same kernel runs the dense (HCA) attention over every row of an array
+// (DS4X README, "Optimization details", the HCA bullet): there an item is a
+// run of consecutive rows rather than a query token, every item reads the one
+// query, and its normalised output goes out in fp32 with its LSE for the
+// split-KV combine over the items.
+//
 // One persistent CTA per SM takes query tokens blockIdx.x, + gridDim.x, ...
 // and runs each query's rows in tiles of 128 through two tcgen05.mma
 // (kind::f16, fp16 operands, fp32 accumulators in tensor memory):
@@ -112,14 +118,21 @@ struct __align__(1024) ASmem {
   int abort_flag;
 };
 
+// Item qi (a query token, or a dense tile) attends over k rows: idx[qi][0..k),
+// or with idx null the consecutive rows qi k .. qi k + k - 1 (those below
+// n_rows).  Its query is q + qi q_stride (q_stride 0: one query shared by
+// every item); its normalised output goes to out as bf16 or, with out_f32 set,
+// to out_f32 in fp32 (the split-KV partials of the dense attention).
 struct PrefillAttnArgs {
   const uint8_t *kv;
   int64_t n_rows;
-  const int32_t *idx;  // [T][k]
+  const int32_t *idx;  // [T][k], or null (dense items)
   int32_t T, k;
   float scale;
-  const uint16_t *q;   // bf16 [T][64][512]
-  uint16_t *out;       // bf16 [T][64][512]
+  const uint16_t *q;   // bf16 [64][512] per item, q_stride elements apart
+  int64_t q_stride;
+  uint16_t *out;       // bf16 [T][64][512] (unused when out_f32 is set)
+  float *out_f32;      // fp32 [T][64][512] or null
   float *lse;          // [T][64] or null
 };
 
@@ -228,7 +241,12 @@ __device__ __forceinline__ void load_tile_words(const PrefillAttnArgs &a, int32_
 // Lane L's row of query qi: row 8 warp + L % 8 of tile L / 8 (-1 past k).
 __device__ __forceinline__ int32_t query_row(const PrefillAttnArgs &a, int qi, int warp, int lane) {
   const int pos = kTile * (lane >> 3) + 8 * warp + (lane & 7);
-  return pos < a.k ? __ldg(a.idx + int64_t(qi) * a.k + pos) : -1;
+  if (pos >= a.k) return -1;
+  if (a.idx == nullptr) {  // dense item: the array's rows qi k + pos (n_rows < 2^31)
+    const int64_t r = int64_t(qi) * a.k + pos;
+    return r < a.n_rows ? int32_t(r) : -1;
+  }
+  return __ldg(a.idx + int64_t(qi) * a.k + pos);
 }
 
 // The row's 7 scale bytes (a skipped row reads row 0's, dropped by pack_scales).
@@ -250,7 +268,7 @@ __device__ __forceinline__ void pack_scales(const PrefillAttnArgs &a, int32_t ro
 // (cp.async, 16 bytes a copy) to their Q' places; the thread waits for its
 // own copies before it converts them.
 __device__ __forceinline__ void copy_query_async(ASmem &sm, const PrefillAttnArgs &a, int qi, int qh, int qb) {
-  const uint16_t *src = a.q + (int64_t(qi) * kHeads + qh) * kDim + 64 * qb;
+  const uint16_t *src = a.q + int64_t(qi) * a.q_stride + int64_t(qh) * kDim + 64 * qb;
 #pragma unroll
   for (int c = 0; c < 8; ++c)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sm.qs + q_off(qh, 8 * qb + c))),
@@ -304,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   // scale bytes 0-3 / 4-6 (the raw query values are copied to Q''s places)
   int32_t rowm = -1;
   uint32_t sc0 = 0, sc1 = 0;
+  // Launched as a programmatic dependent: nothing above touches global memory;
+  // wait here for the previous kernel.  Kernels launched as dependents of this
+  // one may be scheduled from now on (they too wait for its completion).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (int(blockIdx.x) < a.T) {  // the first query's inputs (later queries' arrive during the previous epilogue)
     copy_query_async(sm, a, blockIdx.x, qh, qb);
     rowm = query_row(a, blockIdx.x, warp, lane);
@@ -312,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     pack_scales(a, rowm, b, sc0, sc1);
   }
   for (int qi = blockIdx.x; qi < a.T && !aborted; qi += gridDim.x, ++qn) {
-    const int32_t *idxq = a.idx + int64_t(qi) * a.k;
     int *sbq = sm.sb[qn & 1];
+    uint32_t raw[8][5];  // the words of the warp's 8 rows of the next tile to widen (tile 0's
+    load_tile_words(a, rowm, 0, n_tiles, lane, raw);  // arrive while S_b is found and Q' converted)
     if (named_bar_or(1, kThreads, !ok)) break;  // the previous query's readers of Q', sb[(qn + 1) & 1] are done
     if (tid < 8) sm.sb[(qn + 1) & 1][tid] = tid < kNopeBlocks ? 0 : 127;  // for the next query
     if (!row_ok(a, rowm) && rowm != -1) atomicExch(&hdr->status, int32_t(DS4X_EDEVICE));
@@ -323,8 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
       if (lane == 0 && m > 0) atomicMax(&sbq[b], int(m));
     }
     if (named_bar_or(1, kThreads, !ok)) break;
-    uint32_t raw[8][5];  // the words of the warp's 8 rows of the next tile to widen (tile 0's
-    load_tile_words(a, rowm, 0, n_tiles, lane, raw);  // arrive while Q' is converted)
     // the lane's row's fp16 factors 2^(s_b - S_b): blocks 2 i (low half) and 2 i + 1 of fac[i]
     uint32_t fac[4];
 #pragma unroll
@@ -569,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     // the next query's scale bytes and values are requested now and used after the output
     const bool more = qi + int(gridDim.x) < a.T;
     uint32_t scb_next[kNopeBlocks];  // packed after the output (their loads are in flight meanwhile)
-    load_scale_bytes(a, rowm_next, scb_next);
+    if (more) load_scale_bytes(a, rowm_next, scb_next);
     if (more) copy_query_async(sm, a, qi + int(gridDim.x), qh, qb);  // Q''s buffer is free: the last first MMA is done
     float *red = &sm.red[0][0];
     if ((lane & 1) == 0) red[qd * kHeads + 16 * hg + hl] = wsum;
@@ -579,33 +601,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     for (int i = 0; i < 16; ++i) {
       const int hh = 16 * hg + i;
       const float tot = (red[hh] + red[kHeads + hh]) + (red[2 * kHeads + hh] + red[3 * kHeads + hh]);
-      inv[i] = tot > 0.0f ? 1.0f / tot : 0.0f;
-      if (a.lse != nullptr && qd == 0 && lane == i)
-        a.lse[int64_t(qi) * kHeads + hh] = tot > 0.0f ? (m_ref[i] + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+      inv[i] = tot > 0.0f ? __frcp_rn(tot) : 0.0f;  // = 1 / tot, correctly rounded
     }
-    // o as bf16 [head][dim] in V''s space (free once the last second MMA is done),
-    // then out with 16-byte stores
-    uint16_t *os = reinterpret_cast<uint16_t *>(sm.kv);
+    // the LSE of head 16 hg + hl, from the even lanes of the first quadrant's warps
+    // (m_lane is that head's reference maximum, the same value as m_ref[hl])
+    if (a.lse != nullptr && qd == 0 && (lane & 1) == 0) {
+      const int hh = 16 * hg + hl;
+      const float tot = (red[hh] + red[kHeads + hh]) + (red[2 * kHeads + hh] + red[3 * kHeads + hh]);
+      a.lse[int64_t(qi) * kHeads + hh] = tot > 0.0f ? (m_lane + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+    }
+    if (a.out_f32 != nullptr) {
+      // fp32 [head][dim] straight from the accumulator: a warp's store is 32
+      // consecutive dims of one head
+      float *of = a.out_f32 + int64_t(qi) * kHeads * kDim;
 #pragma unroll 1
-    for (int mi = 0; mi < kDim / 128; ++mi) {
-      uint32_t ov[16];
-      tc_ld_x16(tmem + lane_base + kOCol + 64u * mi + 16u * hg, ov);
-      tc_wait_ld();
-      const int d = 128 * mi + 32 * qd + lane;
-      const float fb = ldexpf(1.0f, sbq[d >> 6] - 127);
+      for (int mi = 0; mi < kDim / 128; ++mi) {
+        uint32_t ov[16];
+        tc_ld_x16(tmem + lane_base + kOCol + 64u * mi + 16u * hg, ov);
+        tc_wait_ld();
+        const int d = 128 * mi + 32 * qd + lane;
+        const float fb = ldexpf(1.0f, sbq[d >> 6] - 127);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        os[(16 * hg + i) * kDim + d] = f32_to_bf16_rn((__uint_as_float(ov[i]) * inv[i]) * fb);
-    }
-    tc_fence_before();
-    named_bar_sync(2, kThreads);
-    {
+        for (int i = 0; i < 16; ++i) of[(16 * hg + i) * kDim + d] = (__uint_as_float(ov[i]) * inv[i]) * fb;
+      }
+      tc_fence_before();
+    } else {
+      // o as bf16 [head][dim] in V''s space (free once the last second MMA is done),
+      // then out with 16-byte stores
+      uint16_t *os = reinterpret_cast<uint16_t *>(sm.kv);
+#pragma unroll 1
+      for (int mi = 0; mi < kDim / 128; ++mi) {
+        uint32_t ov[16];
+        tc_ld_x16(tmem + lane_base + kOCol + 64u * mi + 16u * hg, ov);
+        tc_wait_ld();
+        const int d = 128 * mi + 32 * qd + lane;
+        const float fb = ldexpf(1.0f, sbq[d >> 6] - 127);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          os[(16 * hg + i) * kDim + d] = f32_to_bf16_rn((__uint_as_float(ov[i]) * inv[i]) * fb);
+      }
+      tc_fence_before();
+      named_bar_sync(2, kThreads);
       const uint4 *s4 = reinterpret_cast<const uint4 *>(sm.kv);
       uint4 *o4 = reinterpret_cast<uint4 *>(a.out + int64_t(qi) * kHeads * kDim);
 #pragma unroll
       for (int c = 0; c < kHeads * kDim * 2 / 16 / kThreads; ++c) o4[tid + c * kThreads] = s4[tid + c * kThreads];
     }
-    pack_scales(a, rowm_next, scb_next, sc0, sc1);
+    if (more) pack_scales(a, rowm_next, scb_next, sc0, sc1);
     rowm = rowm_next;
   }
   if (aborted || !ok) {  // thread 0: no MMA may still write this CTA's memory when it exits
@@ -625,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
 
 size_t attn_prefill_ws_bytes() { return kWsHeaderBytes; }
 
-cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
-                                int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
-                                cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_items(const PrefillAttnArgs &a, void *ws, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   // the dynamic shared memory is at least 16-byte aligned: room to round it up to 1024
   const int smem = int(sizeof(ASmem)) + 1024 - 16;
@@ -638,10 +680,37 @@ cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const in
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  PrefillAttnArgs a{kv_rows, n_rows, idx, n_queries, k, scale, q, out, lse};
-  const int grid = n_queries < sms ? n_queries : sms;
-  attn_prefill_kernel<<<grid, kThreads, smem, stream>>>(a, reinterpret_cast<WsHeader *>(ws));
-  return cudaGetLastError();
+  // programmatic stream serialisation: the CTAs may be scheduled while the
+  // previous kernel finishes; they wait for it before touching global memory
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(a.T < sms ? a.T : sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_prefill_kernel, a, reinterpret_cast<WsHeader *>(ws));
+}
+
+}  // namespace
+
+cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
+                                int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
+                                cudaStream_t stream) {
+  const PrefillAttnArgs a{kv_rows, n_rows, idx, n_queries, k, scale, q, int64_t(kHeads) * kDim, out, nullptr, lse};
+  return launch_items(a, ws, stream);
+}
+
+cudaError_t launch_attn_dense_items(const uint8_t *kv_rows, int64_t n_rows, int32_t rows_per_item, int32_t items,
+                                    const uint16_t *q, float scale, float *out_f32, float *lse, void *ws,
+                                    cudaStream_t stream) {
+  if (rows_per_item < 1 || rows_per_item > DS4X_TOPK_MAX || items < 1 || n_rows > int64_t(INT32_MAX))
+    return cudaErrorInvalidValue;
+  const PrefillAttnArgs a{kv_rows, n_rows, nullptr, items, rows_per_item, scale, q, 0, nullptr, out_f32, lse};
+  return launch_items(a, ws, stream);
 }
 
 }  // namespace ds4x

@@ -145,10 +145,13 @@ struct AttnBatch {
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
 size_t attn_decode_ws_bytes(int32_t k);
 
-// Dense attention over every row [0, n_rows) (one query): 512-row tiles as
-// the items of one attention launch (fp32 partials), then a finalize.
+// Dense attention over every row [0, n_rows) (one query): items of
+// consecutive rows (dense_rows_per_item: 128, 256, 384 or 512, the fewest
+// that keep the items at 256 or fewer up to 131,072 rows) through the
+// tensor-core attention kernel (fp32 partials), then a finalize.
 constexpr int64_t kDenseMaxTiles = 8192;  // rows up to 8192 * 512
 static_assert(kDenseMaxTiles * DS4X_TOPK_MAX == DS4X_DENSE_MAX_ROWS, "the ABI's row limit");
+int32_t dense_rows_per_item(int64_t n_rows);
 size_t dense_attn_ws_bytes(int64_t n_rows);
 cudaError_t launch_dense_attn(const uint8_t *kv_rows, int64_t n_rows, const uint16_t *q, float scale, uint16_t *out,
                               float *lse, void *ws, cudaStream_t stream);
@@ -176,6 +179,12 @@ size_t attn_prefill_ws_bytes();
 cudaError_t launch_attn_prefill(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx, int32_t n_queries,
                                 int32_t k, const uint16_t *q, float scale, uint16_t *out, float *lse, void *ws,
                                 cudaStream_t stream);
+// The same kernel over `items` dense items of rows_per_item consecutive rows
+// each (item i: rows i rows_per_item .. below n_rows), all with the one query
+// q, writing each item's normalised fp32 output [64][512] and LSE [64].
+cudaError_t launch_attn_dense_items(const uint8_t *kv_rows, int64_t n_rows, int32_t rows_per_item, int32_t items,
+                                    const uint16_t *q, float scale, float *out_f32, float *lse, void *ws,
+                                    cudaStream_t stream);
 // Kernel-side copy (device or GPU-addressable pinned host memory on either side).
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 cudaError_t launch_attn_decode(const uint8_t *kv_rows, int64_t n_rows, const int32_t *idx,

@@ -405,8 +405,13 @@ int ds4x_sparse_attn_decode_noalloc(const uint8_t *kv_rows, int64_t n_rows, cons
  *   lse_h = log sum_t e^(l_ht)
  *
  * with v_t the dequantised row as in ds4x_sparse_attn_decode.  Computed as
- * 512-row tiles (each one attention item writing its normalised fp32 output
- * and LSE into the workspace), then a log-sum-exp combine over the tiles.
+ * items of R consecutive rows, R = 128 * min(4, max(1, ceil(n_rows /
+ * 32768))) (128 rows up to 32,768 rows, so 64 items at 8192 rows), each
+ * through the tensor-core kernel of ds4x_sparse_attn_prefill (with its
+ * numerics, the block scales' range taken over the item's rows) writing its
+ * normalised fp32 output and LSE into the workspace, then a log-sum-exp
+ * combine over the items.  Workspace: 256 + items * (256 + 131072) bytes,
+ * items = ceil(n_rows / R).
  *
  *   kv_rows   u8 [n_rows][583]
  *   n_rows    1 .. DS4X_DENSE_MAX_ROWS

@@ -148,9 +148,11 @@ def test_prefill_scorer_argument_checks(lib):
 def test_dense_attention_argument_checks(lib):
     s = ctypes.c_float(0.044)
     wsz = lib.ds4x_dense_attn_decode_workspace
-    # header, tile LSEs (64 floats a tile, rounded up to 256 bytes), tile outputs (64 x 512 floats a tile)
-    for n, tiles in [(1, 1), (512, 1), (513, 2), (8192, 16), (100000, 196)]:
-        assert wsz(n) == 256 + ((tiles * 64 * 4 + 255) // 256) * 256 + tiles * 64 * 512 * 4, n
+    # header, item LSEs (64 floats an item, rounded up to 256 bytes), item outputs (64 x 512 floats an
+    # item); items of 128 rows up to 32,768 rows, then 256, 384 and 512 rows
+    for n, items in [(1, 1), (128, 1), (129, 2), (8192, 64), (32768, 256), (32769, 129), (65536, 256),
+                     (65537, 171), (98305, 193), (100000, 196), (8192 * 512, 8192)]:
+        assert wsz(n) == 256 + ((items * 64 * 4 + 255) // 256) * 256 + items * 64 * 512 * 4, n
     f = lib.ds4x_dense_attn_decode
     ws = wsz(8192)
     assert f(None, 8192, FAKE, s, FAKE, None, FAKE, ws, None) == -1
