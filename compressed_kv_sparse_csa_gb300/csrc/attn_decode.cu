@@ -229,8 +229,11 @@ attn_decode_kernel(AttnBatch ab, WsHeader *hdr) {
     }
   }
   // Launched as a programmatic dependent of the previous kernel (the scorer
-  // that wrote idx): everything above reads no input; wait for it here.
+  // that wrote idx): everything above reads no input; wait for it here.  Its
+  // own dependents (a finalize, a copy of the output) may be scheduled from
+  // now on; they wait for its completion.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid < kRows) {
     const int j = split * kRows + tid;
     int64_t r = -1;

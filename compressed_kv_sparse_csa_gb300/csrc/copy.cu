@@ -3,6 +3,8 @@
 // decode loop whose inputs and results live in pinned host memory can move
 // them with this kernel inside its CUDA graph instead of copy-engine copies,
 // whose hand-over to and from the kernels costs several microseconds each.
+// Launched as a programmatic dependent of the previous kernel (it waits for it
+// before touching memory), and lets its own dependents be scheduled at once.
 #include "ds4x_internal.cuh"
 
 namespace ds4x {
@@ -13,6 +15,8 @@ constexpr int kCopyThreads = 256;
 __global__ void __launch_bounds__(kCopyThreads) copy16_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
                                                               size_t n16, uint8_t *__restrict__ dst_tail,
                                                               const uint8_t *__restrict__ src_tail, uint32_t tail) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t stride = size_t(gridDim.x) * blockDim.x;
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
   if (blockIdx.x == 0 && threadIdx.x < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x];
@@ -25,10 +29,18 @@ cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t s
   const uint32_t tail = uint32_t(bytes - 16 * n16);
   const size_t want = (n16 + kCopyThreads - 1) / kCopyThreads;
   const int grid = int(want < 1 ? 1 : (want > 1024 ? 1024 : want));
-  copy16_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), n16,
-                                                    static_cast<uint8_t *>(dst) + 16 * n16,
-                                                    static_cast<const uint8_t *>(src) + 16 * n16, tail);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kCopyThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, copy16_kernel, static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), n16,
+                            static_cast<uint8_t *>(dst) + 16 * n16, static_cast<const uint8_t *>(src) + 16 * n16,
+                            tail);
 }
 
 }  // namespace ds4x

@@ -33,6 +33,9 @@ cache_append_kernel(uint8_t *__restrict__ kv_rows, uint8_t *__restrict__ idx_row
                     const float *__restrict__ kv_in, const float *__restrict__ idx_in,
                     int64_t n) {
   __shared__ __align__(16) uint32_t stage[kWarps][(DS4X_KV_ROW_BYTES + 3) / 4];
+  // launched as a programmatic dependent: the previous kernel (say the copy of
+  // the inputs) is complete and visible past this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t row = int64_t(blockIdx.x) * kWarps + warp;
@@ -87,9 +90,16 @@ cudaError_t launch_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t pos
                                 const float *kv_in, const float *idx_in, int64_t n,
                                 cudaStream_t stream) {
   const int64_t blocks = (n + kWarps - 1) / kWarps;
-  cache_append_kernel<<<dim3(unsigned(blocks)), kWarps * 32, 0, stream>>>(kv_rows, idx_rows, pos,
-                                                                          kv_in, idx_in, n);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cache_append_kernel, kv_rows, idx_rows, pos, kv_in, idx_in, n);
 }
 
 }  // namespace ds4x
