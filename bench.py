@@ -8,10 +8,12 @@ heads x 128, 64 attention heads x 512), synthetic N(0,1) data packed by the
 library's own cache writer.
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
-graphs (one graph per layer cache), bracketed by a barrier and a device
-synchronise, timed with CUDA events on the launching stream.  Inputs larger
-than L2: the steps rotate over L layer caches (L x 71.3 MB of indexer rows
-> 4 x the 129 MB L2), so every step streams its rows from HBM.
+graphs, bracketed by a barrier and a device synchronise, timed with CUDA
+events on the launching stream.  The steps rotate over L layer caches, and
+the L layer steps of a token are one CUDA graph (K mod L steps are replayed
+from one-step graphs); the time with one graph per step is reported beside
+it.  Inputs larger than L2: L x 71.3 MB of indexer rows > 4 x the 129 MB
+L2, so every step streams its rows from HBM.
 
 Printed: one JSON line (rank 0).  `value` is compressed rows scored per second
 over the whole job; `roofline` is the dominant kernel (the scorer entry
@@ -424,14 +426,21 @@ def main():
             step(i % L)
     stream.synchronize()
 
+    # The L layer steps of a decode token run back to back, as one CUDA graph
+    # (a server captures a token's layers together); one graph per layer step
+    # is kept for the remainder of K / L and for the per-step-graph figure.
     def capture(score_only):
-        graphs = []
+        singles = []
         for l in range(L):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step(l, score_only)
-            graphs.append(g)
-        return graphs
+            singles.append(g)
+        whole = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(whole, stream=stream):
+            for l in range(L):
+                step(l, score_only)
+        return singles, whole
 
     step_graphs = capture(False)
     score_graphs = capture(True)
@@ -440,10 +449,14 @@ def main():
         if dist is not None:
             dist.barrier()
 
-    def timed(graphs, k):
+    def timed(graphs, k, per_step_graphs=False):
+        """Exactly k steps: k // L replays of the L-step graph and the first
+        k % L single-step graphs (or k single-step graphs)."""
+        singles, whole = graphs
         with torch.cuda.stream(stream):
-            for g in graphs:  # untimed replay of each graph once
+            for g in singles:  # untimed replay of each graph once
                 g.replay()
+            whole.replay()
         stream.synchronize()
         barrier()
         torch.cuda.synchronize()
@@ -451,8 +464,14 @@ def main():
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):  # replay() launches on the current stream
             e0.record(stream)
-            for i in range(k):
-                graphs[i % L].replay()
+            if per_step_graphs:
+                for i in range(k):
+                    singles[i % L].replay()
+            else:
+                for _ in range(k // L):
+                    whole.replay()
+                for i in range(k % L):
+                    singles[i].replay()
             e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -462,6 +481,7 @@ def main():
         ms_total = timed(step_graphs, args.steps)
     clocks = clk.summary()
     ms_score = timed(score_graphs, args.steps)
+    ms_total_1 = timed(step_graphs, args.steps, per_step_graphs=True)  # for comparison only
 
     # ---- end to end through the public API, host buffers, copies inside.
     # A step's inputs (the new row's 512 + 128 values, both queries, the head
@@ -517,21 +537,25 @@ def main():
         with torch.cuda.graph(g, stream=stream):
             e2e_calls(l)
         e2e_graphs.append(g)
-
-    def e2e_step(l):
-        e2e_graphs[l].replay()
+    e2e_whole = torch.cuda.CUDAGraph()  # a token's L layer steps, each with its copies
+    with torch.cuda.graph(e2e_whole, stream=stream):
+        for l in range(L):
+            e2e_calls(l)
 
     with torch.cuda.stream(stream):
         for i in range(3):
-            e2e_step(i % L)
+            e2e_graphs[i % L].replay()
+        e2e_whole.replay()
         stream.synchronize()
         barrier()
         t0 = time.perf_counter()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(e2e_steps):
-            e2e_step(i % L)
+        for _ in range(e2e_steps // L):
+            e2e_whole.replay()
+        for i in range(e2e_steps % L):
+            e2e_graphs[i].replay()
         e1.record(stream)
         stream.synchronize()
         barrier()
@@ -540,7 +564,8 @@ def main():
     ms_step = ms_total / args.steps
     ms_sc = ms_score / args.steps
     ms_e2e_step = ms_e2e / e2e_steps
-    ms_step, ms_sc, ms_e2e_step = max_over_ranks([ms_step, ms_sc, ms_e2e_step], dist, dev)
+    ms_step_1 = ms_total_1 / args.steps
+    ms_step, ms_sc, ms_e2e_step, ms_step_1 = max_over_ranks([ms_step, ms_sc, ms_e2e_step, ms_step_1], dist, dev)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -568,6 +593,8 @@ def main():
                    "layer_caches_rotated": L,
                    "l2": f"inputs larger than L2: {L} layer caches x {68 * n / 1e6:.1f} MB indexer rows rotated",
                    "us_per_layer": ms_step * 1e3,
+                   "graphs": f"the {L} layer steps of a token as one CUDA graph (K mod {L} steps as one-step graphs)",
+                   "us_per_layer_one_graph_per_step": ms_step_1 * 1e3,
                    "achieved_step_gbs": step_bytes(n) / (ms_step * 1e-3) / 1e9,
                    "step_bytes": step_bytes(n),
                    "step_roofline_frac": (step_bytes(n) / (ms_step * 1e-3) / 1e9) / peak,
@@ -580,9 +607,10 @@ def main():
         "e2e": {"value": job_value(world, n, ms_e2e_step), "unit": "compressed rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": ms_e2e_step,
-                "path": "per step one CUDA graph of the public calls: ds4x_copy_async of the packed inputs from "
-                        "pinned host memory (a kernel), ds4x_cache_append, ds4x_csa_decode_step (score + top-512, "
-                        "attention), ds4x_copy_async of the output and indices to pinned host memory"},
+                "path": f"the public calls of {L} layer steps as one CUDA graph, each step: ds4x_copy_async of "
+                        "its packed inputs from pinned host memory (a kernel), ds4x_cache_append, "
+                        "ds4x_csa_decode_step (score + top-512, attention), ds4x_copy_async of its output and "
+                        "indices to pinned host memory"},
         "gpu_launches": args.steps * (launches_per_step["score"] + launches_per_step["attn"]),
         "clocks": clocks,
     }
