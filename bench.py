@@ -657,6 +657,56 @@ def _timed_graph(torch, stream, graphs, steps, warmup=3):
     return e0.elapsed_time(e1) / steps  # ms per step
 
 
+GROUP = 8  # decode steps per CUDA graph (a token's layers back to back)
+
+
+def _step_graphs(torch, stream, calls):
+    """One-step graphs of each call (a closure launching one step) and graphs
+    of GROUP consecutive steps (calls taken cyclically)."""
+    singles = []
+    for f in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            f()
+        singles.append(g)
+    groups = []
+    for j0 in range(0, len(calls), GROUP):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(j0, j0 + GROUP):
+                calls[j % len(calls)]()
+        groups.append(g)
+    return singles, groups
+
+
+def _timed_steps(torch, stream, graphs, steps, warmup=3, per_step_graphs=False):
+    """ms per step over exactly `steps` steps: steps // GROUP group replays
+    and steps % GROUP one-step replays (or one-step graphs throughout)."""
+    singles, groups = graphs
+    with torch.cuda.stream(stream):  # untimed warm-up replays
+        for i in range(max(warmup, len(singles))):
+            singles[i % len(singles)].replay()
+        for g in groups:
+            g.replay()
+    stream.synchronize()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        if per_step_graphs:
+            for i in range(steps):
+                singles[i % len(singles)].replay()
+        else:
+            for i in range(steps // GROUP):
+                groups[i % len(groups)].replay()
+            for i in range(steps % GROUP):
+                singles[i % len(singles)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_sessions(args):
     """16 independent decode sessions (lengths uniform on [8192, 65536],
     seeded), one batched scorer launch and one batched attention launch per
@@ -709,17 +759,13 @@ def run_sessions(args):
         for i in range(args.warmup):
             step(layers[i % L])
     stream.synchronize()
-    graphs, sgraphs = [], []
-    for c in layers:
-        for lst, so in ((graphs, False), (sgraphs, True)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(c, so)
-            lst.append(g)
+    graphs = _step_graphs(torch, stream, [lambda c=c: step(c) for c in layers])
+    sgraphs = _step_graphs(torch, stream, [lambda c=c: step(c, True) for c in layers])
     steps = min(args.steps, 1000)
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        ms = _timed_graph(torch, stream, graphs, steps, args.warmup)
-    ms_sc = _timed_graph(torch, stream, sgraphs, steps, args.warmup)
+        ms = _timed_steps(torch, stream, graphs, steps, args.warmup)
+    ms_sc = _timed_steps(torch, stream, sgraphs, steps, args.warmup)
+    ms_1 = _timed_steps(torch, stream, graphs, steps, args.warmup, per_step_graphs=True)
     total = int(lens.sum())
     step_b = sum(step_bytes(int(x)) for x in lens)
     peak, kind = measured_peak()
@@ -732,6 +778,7 @@ def run_sessions(args):
         "config": {"workload": "16 decode sessions, lengths uniform on [8192, 65536] (seed 1003), batch 1 each",
                    "rows_total": total, "lengths": [int(x) for x in lens], "top_k": K_TOP, "layer_copies": L,
                    "us_per_step": ms * 1e3, "step_bytes": step_b,
+                   "graphs": f"{GROUP} steps per CUDA graph (K mod {GROUP} as one-step graphs)", "us_per_step_one_graph_per_step": ms_1 * 1e3,
                    "step_roofline_frac": step_b / (ms * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": "ds4x_index_score_topk_batched", "bound": "hbm",
                      "achieved": sb / (ms_sc * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -768,15 +815,11 @@ def run_hca(args):
         for i in range(args.warmup):
             step(layers[i % L])
     stream.synchronize()
-    graphs = []
-    for c in layers:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(c)
-        graphs.append(g)
+    graphs = _step_graphs(torch, stream, [lambda c=c: step(c) for c in layers])
     steps = min(args.steps, 2000)
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        ms = _timed_graph(torch, stream, graphs, steps, args.warmup)
+        ms = _timed_steps(torch, stream, graphs, steps, args.warmup)
+    ms_1 = _timed_steps(torch, stream, graphs, steps, args.warmup, per_step_graphs=True)
     peak, kind = measured_peak()
     algo = n * 583 + 2 * 64 * 512 * 2  # the rows, the query, the output
     print(json.dumps({
@@ -786,7 +829,8 @@ def run_hca(args):
         "dtype": "bf16-in/fp32-acc (E4M3/FP16 packed rows)", "data": "synthetic",
         "config": {"workload": "dense attention over 8192 ratio-128 rows (1M-token context), 64 heads",
                    "n_rows": n, "layer_copies": L, "l2": "inputs larger than L2: 40 x 4.8 MB rotated",
-                   "us_per_step": ms * 1e3},
+                   "us_per_step": ms * 1e3,
+                   "graphs": f"{GROUP} steps per CUDA graph (K mod {GROUP} as one-step graphs)", "us_per_step_one_graph_per_step": ms_1 * 1e3},
         "roofline": {"kernel": "ds4x_dense_attn_decode", "bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9,
                      "peak": peak, "unit": "GB/s", "frac": algo / (ms * 1e-3) / 1e9 / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": algo, "peak_kind": kind},
@@ -827,15 +871,11 @@ def run_window(args):
         for i in range(args.warmup):
             step(items[i % L])
     stream.synchronize()
-    graphs = []
-    for c in items:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(c)
-        graphs.append(g)
+    graphs = _step_graphs(torch, stream, [lambda c=c: step(c) for c in items])
     steps = min(args.steps, 2000)
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        ms = _timed_graph(torch, stream, graphs, steps, args.warmup)
+        ms = _timed_steps(torch, stream, graphs, steps, args.warmup)
+    ms_1 = _timed_steps(torch, stream, graphs, steps, args.warmup, per_step_graphs=True)
     peak, kind = measured_peak()
     # the selected and the window rows, the index list, the query, the output
     algo = (K_TOP + w) * 583 + K_TOP * 4 + 2 * 64 * 512 * 2
@@ -846,7 +886,8 @@ def run_window(args):
         "dtype": "bf16-in/fp32-acc (E4M3/FP16 packed rows)", "data": "synthetic",
         "config": {"workload": "512 selected rows of a 1,048,576-row cache + 256 live raw-window rows, 64 heads",
                    "n_rows": n, "window": w, "rotated": L,
-                   "l2": "selected rows random over a 611 MB cache (above L2); 8 rings and index lists rotated"},
+                   "l2": "selected rows random over a 611 MB cache (above L2); 8 rings and index lists rotated",
+                   "graphs": f"{GROUP} steps per CUDA graph (K mod {GROUP} as one-step graphs)", "us_per_step_one_graph_per_step": ms_1 * 1e3},
         "roofline": {"kernel": "ds4x_window_sparse_attn_decode", "bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9,
                      "peak": peak, "unit": "GB/s", "frac": algo / (ms * 1e-3) / 1e9 / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": algo, "peak_kind": kind},
