@@ -424,9 +424,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) prefill_topk_kernel(PrefillArg
       const int64_t want = (2 * int64_t(need) * ns + n - 1) / n + 4;  // sample rank of T (1-based)
       const int rt = int(want < ns ? want : ns) - 1;
       if (tid == rt) sm.red_key[0] = srt_s;
-      if (tid == 0) sm.n_list = 0;
       bar512();
       const unsigned long long t_key = sm.red_key[0];
+      // Each warp appends into its own segment of the list with a running
+      // count (the same in every lane: no shared atomics, which serialise a
+      // pass this long); a segment's unused slots are zero keys (padding,
+      // which the selection skips).  A warp with more keys than its segment
+      // holds sends the token to the histogram path below.
+      constexpr int kSeg = kSelCap / (kSelThreads / 32);  // 576 slots a warp
+      unsigned long long *seg = sm.list + warp * kSeg;
+      const unsigned lt = (1u << lane) - 1u;
+      int wcount = 0;
       for (int64_t t0 = 0; t0 < n4; t0 += kUnroll * kSelThreads) {
         float4 v[kUnroll];
 #pragma unroll
@@ -442,15 +450,24 @@ __global__ void __launch_bounds__(kSelThreads, 2) prefill_topk_kernel(PrefillArg
           for (int c = 0; c < 4; ++c) {
             const unsigned long long key = e0 + c < n ? make_key(x[c], uint32_t(e0 + c)) : 0ull;
             const bool take = key != 0ull && key >= t_key;
-            const int p = warp_append(&sm.n_list, take);
-            if (take && p < kSelCap) sm.list[p] = key;
+            const unsigned msk = __ballot_sync(0xffffffffu, take);
+            const int p = wcount + __popc(msk & lt);
+            if (take && p < kSeg) seg[p] = key;
+            wcount += __popc(msk);
           }
         }
       }
+      for (int i = wcount + lane; i < kSeg; i += 32) seg[i] = 0ull;
+      if (lane == 0) sm.wsum[warp] = wcount;
       bar512();
-      const int cnt = sm.n_list;
-      if (cnt >= need && cnt <= kSelCap) {
-        m = select_top(sm.list, cnt, need, sm.best, sm.hist, sm.sortbuf, sm.sel, tid);
+      int cnt = 0;
+      bool over = false;
+      for (int w = 0; w < kSelThreads / 32; ++w) {
+        cnt += sm.wsum[w];
+        over = over || sm.wsum[w] > kSeg;
+      }
+      if (cnt >= need && !over) {
+        m = select_top(sm.list, kSelCap, need, sm.best, sm.hist, sm.sortbuf, sm.sel, tid);
         need = 0;
       }
       bar512();
