@@ -50,8 +50,12 @@
 // row per step, lane L converting the row's 4-byte words L + 32 i:
 // coalesced loads, conflict-free swizzled stores), then read S^T (warp w:
 // lanes 32 (w % 4) .., heads 16 (w / 4) ..), run the softmax and write P^T;
-// thread 0 issues each tile's MMAs once a barrier shows every warp's
-// operands written.  A tile's steps run in sequence: widen -> S^T ->
+// lane 0 of warps 0 and 1 issue each tile's MMAs once a barrier shows every
+// warp's operands written, each half of them (S^T as two K halves into two
+// accumulators that the softmax adds; O^T two of its four M tiles each), and
+// each commits to the tile's barriers (two arrivals a phase): one thread
+// alone issues at about half the tensor core's rate for these shapes.  A
+// tile's steps run in sequence: widen -> S^T ->
 // softmax -> O^T; the next tile's row words are requested as soon as this
 // tile's second MMA is issued, so they arrive while it runs.
 //
@@ -77,7 +81,8 @@ constexpr int kTile = 128;                                 // rows per tile
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kOCol = 0;    // O^T: dims 128 i .. as columns 64 i .. 64 i + 63
-constexpr uint32_t kSCol = 256;  // S^T: columns 256 .. 319
+constexpr uint32_t kSCol = 256;  // S^T in two K halves: columns 256 .. 319 (dims 0-255), 320 .. 383
+constexpr int kIssuers = 2;      // lane 0 of warps 0 and 1 issue the MMAs
 constexpr unsigned long long kTimeoutNs = 500ull * 1000 * 1000;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;    // a head's reference maximum moves by more than this only
@@ -284,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   const int n_tiles = (a.k + kTile - 1) / kTile;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.pv_done), 1);
+    mbar_init(smem_u32(&sm.s_full), kIssuers);  // one commit from each issuer
+    mbar_init(smem_u32(&sm.pv_done), kIssuers);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -315,7 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   const int hl = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
   const int qh = tid >> 3, qb = tid & 7;  // Q': head tid / 8, block tid % 8
   uint32_t g = 0;   // tiles so far (the phase of s_full and pv_done)
-  int pending = 0;  // thread 0: 1 = s_full of the current tile committed last, 2 = pv_done of the last tile
+  // the MMA issuers: lane 0 of warps 0 and 1 (issuer ih = warp)
+  const bool issuer = lane == 0 && warp < kIssuers;
+  const int ih = warp;
+  int pending = 0;  // an issuer: 1 = s_full of the current tile committed last, 2 = pv_done of the last tile
   bool ok = true, aborted = false;
   int qn = 0;       // queries so far: sb[qn & 1] is this query's
   // this query's inputs: lane L's row (row 8 warp + L % 8 of tile L / 8) and its
@@ -446,13 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         aborted = true;
         break;
       }
-      if (tid == 0) {
+      if (issuer) {
         tc_fence_after();
-        // K step ks: 32 bytes into panel ks / 4 (the descriptors' address field counts 16 bytes)
+        // issuer ih: K steps 16 ih .. 16 ih + 15 (dims 256 ih ..) into its own accumulator,
+        // columns kSCol + 64 ih; K step ks: 32 bytes into panel ks / 4 (the descriptors'
+        // address field counts 16 bytes)
 #pragma unroll
-        for (int ks = 0; ks < kDim / 16; ++ks)
-          mma_f16_ss(tmem + kSCol, dS_a + uint64_t(1024 * (ks >> 2) + 2 * (ks & 3)),
-                     dS_b + uint64_t(512 * (ks >> 2) + 2 * (ks & 3)), kIdS, ks > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kDim / 16 / kIssuers; ++kk) {
+          const int ks = (kDim / 16 / kIssuers) * ih + kk;
+          mma_f16_ss(tmem + kSCol + 64u * uint32_t(ih), dS_a + uint64_t(1024 * (ks >> 2) + 2 * (ks & 3)),
+                     dS_b + uint64_t(512 * (ks >> 2) + 2 * (ks & 3)), kIdS, kk > 0 ? 1u : 0u);
+        }
         tc_commit(smem_u32(&sm.s_full));
         pending = 1;
       }
@@ -465,9 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         uint32_t sv[16];
         tc_ld_x16(tmem + lane_base + kSCol + 16u * hg, sv);
         tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) l[i] = __uint_as_float(sv[i]);
+        tc_ld_x16(tmem + lane_base + kSCol + 64u + 16u * hg, sv);
+        tc_wait_ld();
         const bool rv0 = sm.rvalid[r_sm] != 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) l[i] = rv0 ? __uint_as_float(sv[i]) * sm.qscale[16 * hg + i] : -INFINITY;
+        for (int i = 0; i < 16; ++i) l[i] = rv0 ? (l[i] + __uint_as_float(sv[i])) * sm.qscale[16 * hg + i] : -INFINITY;
       }
       float *red = &sm.red[0][0];
 #pragma unroll
@@ -536,15 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         aborted = true;
         break;
       }
-      if (tid == 0) {
+      if (issuer) {
         tc_fence_after();
         // M tile mi: panels 2 mi, 2 mi + 1 (32 KB on); K step ks: 16 rows (2 KB) on.  The four
-        // M tiles' accumulators are independent: their MMAs interleave
+        // M tiles' accumulators are independent: issuer ih takes M tiles 2 ih and 2 ih + 1,
+        // their MMAs interleaved
         const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
 #pragma unroll
-          for (int mi = 0; mi < kDim / 128; ++mi) {
+          for (int mj = 0; mj < kDim / 128 / kIssuers; ++mj) {
+            const int mi = (kDim / 128 / kIssuers) * ih + mj;
             const uint64_t ad = dO_a + uint64_t(2048 * mi + 128 * ks);
             mma_f16_ss(tmem + kOCol + 64u * mi, ad, dO_bh + uint64_t(128 * ks), kIdO, ks > 0 ? 1u : acc0);
             mma_f16_ss(tmem + kOCol + 64u * mi, ad, dO_bl + uint64_t(128 * ks), kIdO, 1u);
@@ -650,9 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     if (more) pack_scales(a, rowm_next, scb_next, sc0, sc1);
     rowm = rowm_next;
   }
-  if (aborted || !ok) {  // thread 0: no MMA may still write this CTA's memory when it exits
-    if (tid == 0 && pending == 1) drain_bar(&sm.s_full, (g - 1 + (aborted ? 1 : 0)) & 1);
-    if (tid == 0 && pending == 2) drain_bar(&sm.pv_done, (g - 1) & 1);
+  if (aborted || !ok) {  // the issuers: no MMA may still write this CTA's memory when it exits
+    if (issuer && pending == 1) drain_bar(&sm.s_full, (g - 1 + (aborted ? 1 : 0)) & 1);
+    if (issuer && pending == 2) drain_bar(&sm.pv_done, (g - 1) & 1);
   }
 
   tc_fence_before();
