@@ -433,6 +433,10 @@ __device__ void hist_cuts(const uint32_t *hist, SelShared &sh, int tid, int M) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 score_fused_kernel(ScoreBatch sb, FusedWs *__restrict__ ws) {
+  // Launched as a programmatic dependent of the previous kernel (the append
+  // of the step's new row, or the previous step's attention): its CTAs may be
+  // resident early; nothing is read or written before that kernel completes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x;
@@ -1133,17 +1137,21 @@ cudaError_t launch_score_batch(const ScoreBatch &sb, int64_t tiles_hint, void *w
   // one session: no more CTAs than tiles; a batch: every SM (the kernel splits them)
   const int grid = (tiles_hint > 0 && tiles_hint < cap) ? int(tiles_hint) : cap;
   if (sb.rows_arr != nullptr && grid < sb.n_sess) return cudaErrorInvalidConfiguration;
-  // cooperative: the CTAs of a session meet at a barrier, so all must be resident
+  // cooperative: the CTAs of a session meet at a barrier, so all must be
+  // resident; programmatic stream serialisation: they may be dispatched while
+  // the previous kernel finishes (each waits for it before touching memory)
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = size_t(smem_bytes);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, score_fused_kernel, sb, static_cast<FusedWs *>(ws));
 }
 
