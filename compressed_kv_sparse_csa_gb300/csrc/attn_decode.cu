@@ -733,7 +733,7 @@ cudaError_t launch_finalize(const float *lse_part, const float *o_part, int T, u
   cfg.blockDim = dim3(kFinThreads);
   cfg.dynamicSmemBytes = size_t(T) * sizeof(float);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[1];  // programmatic stream serialisation (the kernel waits first thing)
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;

@@ -29,18 +29,9 @@ cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t s
   const uint32_t tail = uint32_t(bytes - 16 * n16);
   const size_t want = (n16 + kCopyThreads - 1) / kCopyThreads;
   const int grid = int(want < 1 ? 1 : (want > 1024 ? 1024 : want));
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(kCopyThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, copy16_kernel, static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), n16,
-                            static_cast<uint8_t *>(dst) + 16 * n16, static_cast<const uint8_t *>(src) + 16 * n16,
-                            tail);
+  return launch_pdl(copy16_kernel, unsigned(grid), kCopyThreads, 0, stream, static_cast<uint4 *>(dst),
+                    static_cast<const uint4 *>(src), n16, static_cast<uint8_t *>(dst) + 16 * n16,
+                    static_cast<const uint8_t *>(src) + 16 * n16, tail);
 }
 
 }  // namespace ds4x

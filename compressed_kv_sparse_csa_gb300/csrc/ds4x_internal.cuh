@@ -86,6 +86,26 @@ cudaError_t set_max_smem_once(Kernel *kernel, int bytes, std::atomic<uint64_t> &
   return e;
 }
 
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialisation: its CTAs may be scheduled while the previous kernel
+// in the stream finishes; the kernel waits for it (griddepcontrol.wait)
+// before it touches memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------------------------
 // Launchers (host).  Each returns a cudaError_t from cudaGetLastError().
 // ---------------------------------------------------------------------------

@@ -90,16 +90,8 @@ cudaError_t launch_cache_append(uint8_t *kv_rows, uint8_t *idx_rows, int64_t pos
                                 const float *kv_in, const float *idx_in, int64_t n,
                                 cudaStream_t stream) {
   const int64_t blocks = (n + kWarps - 1) / kWarps;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(unsigned(blocks));
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cache_append_kernel, kv_rows, idx_rows, pos, kv_in, idx_in, n);
+  return launch_pdl(cache_append_kernel, unsigned(blocks), kWarps * 32, 0, stream, kv_rows, idx_rows, pos, kv_in, idx_in,
+                    n);
 }
 
 }  // namespace ds4x

@@ -18,6 +18,10 @@ constexpr int kQBlock = 32;
 __global__ void __launch_bounds__(256) quantize_query_kernel(const float *__restrict__ q, int64_t n_vec,
                                                              uint8_t *__restrict__ codes,
                                                              uint8_t *__restrict__ scales) {
+  // launched as a programmatic dependent: the previous kernel is complete and
+  // visible past this wait; the next kernel's CTAs may be scheduled from now on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t v = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (v >= n_vec) return;
@@ -39,8 +43,7 @@ cudaError_t launch_quantize_query(const float *q, int64_t n_vec, uint8_t *codes,
                                   cudaStream_t stream) {
   const int warps = 8;
   const int64_t blocks = (n_vec + warps - 1) / warps;
-  quantize_query_kernel<<<unsigned(blocks), warps * 32, 0, stream>>>(q, n_vec, codes, scales);
-  return cudaGetLastError();
+  return launch_pdl(quantize_query_kernel, unsigned(blocks), warps * 32, 0, stream, q, n_vec, codes, scales);
 }
 
 }  // namespace ds4x

@@ -172,6 +172,10 @@ __device__ __forceinline__ int64_t visible_rows(const PrefillArgs &a, int64_t q)
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_score_kernel(PrefillArgs a, WsHeader *__restrict__ hdr) {
+  // launched as a programmatic dependent: the previous kernel is complete and
+  // visible past this wait; the next kernel's CTAs may be scheduled from now on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   PSmem &sm = *reinterpret_cast<PSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -389,6 +393,10 @@ struct __align__(16) TSmem {
 };
 
 __global__ void __launch_bounds__(kSelThreads, 2) prefill_topk_kernel(PrefillArgs a) {
+  // launched as a programmatic dependent: the previous kernel is complete and
+  // visible past this wait; the next kernel's CTAs may be scheduled from now on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t tsm_raw[];
   TSmem &sm = *reinterpret_cast<TSmem *>((reinterpret_cast<uintptr_t>(tsm_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -661,10 +669,12 @@ cudaError_t launch_score_prefill(const uint8_t *idx_rows, int64_t n_rows, const 
   for (int32_t q0 = 0; q0 < T; q0 += qpl) {
     pa.q0 = q0;
     pa.nq = T - q0 < qpl ? T - q0 : qpl;
-    prefill_score_kernel<<<unsigned((pa.nq + kPair - 1) / kPair), kThreads, size_t(smem_score), stream>>>(pa, hdr);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    prefill_topk_kernel<<<unsigned(pa.nq), kSelThreads, size_t(smem_topk), stream>>>(pa);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(prefill_score_kernel, unsigned((pa.nq + kPair - 1) / kPair), kThreads, size_t(smem_score),
+                        stream, pa, hdr)) != cudaSuccess)
+      return e;
+    if ((e = launch_pdl(prefill_topk_kernel, unsigned(pa.nq), kSelThreads, size_t(smem_topk), stream, pa)) !=
+        cudaSuccess)
+      return e;
   }
   return cudaSuccess;
 }
