@@ -116,6 +116,7 @@ struct __align__(1024) ASmem {
   uint8_t p_lo[kTile * kHeads * 2];
   float red[4][kHeads];              // per-quadrant maxima (each tile), then sums (each query)
   float qscale[kHeads];              // scale * log2(e) * 2^-c_h
+  float hinv[kHeads];                // a query's 1 / (sum of p) per head, for its output
   int sb[2][8];                      // S_b (UE8M0 bytes; [7] = 127 for the RoPE part), by query parity
   uint8_t rvalid[kTile];             // the tile's row j is a selected, in-range row
   unsigned long long s_full, pv_done;
@@ -338,6 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
   if (int(blockIdx.x) < a.T) {  // the first query's inputs (later queries' arrive during the previous epilogue)
     copy_query_async(sm, a, blockIdx.x, qh, qb);
     rowm = query_row(a, blockIdx.x, warp, lane);
+    // the first tile's rows toward L2 while the scale bytes are awaited (lanes 0-7
+    // hold the tile's rows 8 warp + 0..7; lane L < 6 takes the row's L-th 128-byte
+    // line, every address inside the row)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int32_t row = __shfl_sync(0xffffffffu, rowm, k);
+      if (lane < 6 && row_ok(a, row)) {
+        const int64_t o = int64_t(row) * DS4X_KV_ROW_BYTES;
+        const int64_t line = (o & ~int64_t(127)) + 128 * lane;
+        const int64_t at = line > o ? line : o;
+        if (at < o + DS4X_KV_ROW_BYTES) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.kv + at));
+      }
+    }
     uint32_t b[kNopeBlocks];
     load_scale_bytes(a, rowm, b);
     pack_scales(a, rowm, b, sc0, sc1);
@@ -614,20 +628,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
     float *red = &sm.red[0][0];
     if ((lane & 1) == 0) red[qd * kHeads + 16 * hg + hl] = wsum;
     if (named_bar_or(1, kThreads, !ok)) break;
-    float inv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int hh = 16 * hg + i;
-      const float tot = (red[hh] + red[kHeads + hh]) + (red[2 * kHeads + hh] + red[3 * kHeads + hh]);
-      inv[i] = tot > 0.0f ? __frcp_rn(tot) : 0.0f;  // = 1 / tot, correctly rounded
-    }
-    // the LSE of head 16 hg + hl, from the even lanes of the first quadrant's warps
-    // (m_lane is that head's reference maximum, the same value as m_ref[hl])
-    if (a.lse != nullptr && qd == 0 && (lane & 1) == 0) {
+    // each head's sum once, by the even lanes of the first quadrant's warps (lane L:
+    // head 16 hg + hl; m_lane is that head's reference maximum, the same value as
+    // m_ref[hl]): its reciprocal for every thread, and its LSE
+    if (qd == 0 && (lane & 1) == 0) {
       const int hh = 16 * hg + hl;
       const float tot = (red[hh] + red[kHeads + hh]) + (red[2 * kHeads + hh] + red[3 * kHeads + hh]);
-      a.lse[int64_t(qi) * kHeads + hh] = tot > 0.0f ? (m_lane + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+      sm.hinv[hh] = tot > 0.0f ? __frcp_rn(tot) : 0.0f;  // = 1 / tot, correctly rounded
+      if (a.lse != nullptr)
+        a.lse[int64_t(qi) * kHeads + hh] = tot > 0.0f ? (m_lane + log2f(tot)) * 0.6931471805599453f : -INFINITY;
     }
+    named_bar_sync(2, kThreads);
+    float inv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) inv[i] = sm.hinv[16 * hg + i];
     if (a.out_f32 != nullptr) {
       // fp32 [head][dim] straight from the accumulator: a warp's store is 32
       // consecutive dims of one head
