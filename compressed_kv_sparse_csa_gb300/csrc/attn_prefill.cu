@@ -117,12 +117,17 @@ struct __align__(1024) ASmem {
   float red[4][kHeads];              // per-quadrant maxima (each tile), then sums (each query)
   float qscale[kHeads];              // scale * log2(e) * 2^-c_h
   float hinv[kHeads];                // a query's 1 / (sum of p) per head, for its output
+  float tmax[kHeads];                // a tile's maximum per head (log2 units)
   int sb[2][8];                      // S_b (UE8M0 bytes; [7] = 127 for the RoPE part), by query parity
   uint8_t rvalid[kTile];             // the tile's row j is a selected, in-range row
   unsigned long long s_full, pv_done;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// the dynamic shared memory, rounded up to a 1024-byte boundary inside it, fits
+// the 227 KB a CTA may have
+static_assert(sizeof(ASmem) + 1024 - 16 <= 232448, "shared-memory budget");
 
 // Item qi (a query token, or a dense tile) attends over k rows: idx[qi][0..k),
 // or with idx null the consecutive rows qi k .. qi k + k - 1 (those below
@@ -506,12 +511,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         if (lane == i) red[qd * kHeads + 16 * hg + i] = ordered_float(mx);
       }
       named_bar_sync(2, kThreads);
+      // each head's tile maximum once, over the four quadrants (lanes 0-15 of the first
+      // quadrant's warps: head 16 hg + lane), then read by every thread
+      if (qd == 0 && lane < 16) {
+        const int hh = 16 * hg + lane;
+        sm.tmax[hh] = fmaxf(fmaxf(red[hh], red[kHeads + hh]), fmaxf(red[2 * kHeads + hh], red[3 * kHeads + hh]));
+      }
+      named_bar_sync(2, kThreads);
       bool rescale = false;
       float alpha[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int hh = 16 * hg + i;
-        const float mt = fmaxf(fmaxf(red[hh], red[kHeads + hh]), fmaxf(red[2 * kHeads + hh], red[3 * kHeads + hh]));
+        const float mt = sm.tmax[16 * hg + i];
         alpha[i] = 1.0f;
         if (mt > m_ref[i] + kLazy) {
           alpha[i] = m_ref[i] == -INFINITY ? 0.0f : ex2(m_ref[i] - mt);
@@ -520,8 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(PrefillAttnAr
         }
       }
       {  // the same decision for this lane's head of the sum
-        const int hh = 16 * hg + hl;
-        const float mt = fmaxf(fmaxf(red[hh], red[kHeads + hh]), fmaxf(red[2 * kHeads + hh], red[3 * kHeads + hh]));
+        const float mt = sm.tmax[16 * hg + hl];
         if (mt > m_lane + kLazy) {
           wsum *= m_lane == -INFINITY ? 0.0f : ex2(m_lane - mt);
           m_lane = mt;
