@@ -293,6 +293,12 @@ def cpu_baseline(n_rows=262144, reps=5):
                                         f"distribution, 1 thread; {t1:.2f} s each"}}
 
 
+def replay_plan(k, group):
+    """Graph replays that run exactly k steps when a group graph runs `group`
+    steps: (group replays, one-step replays), k // group and k % group."""
+    return k // group, k % group
+
+
 def max_over_ranks(values, dist, device):
     """Each timed quantity's maximum over the ranks (the job is as slow as
     its slowest replica); unchanged on one process."""
@@ -468,9 +474,10 @@ def main():
                 for i in range(k):
                     singles[i % L].replay()
             else:
-                for _ in range(k // L):
+                n_whole, n_single = replay_plan(k, L)
+                for _ in range(n_whole):
                     whole.replay()
-                for i in range(k % L):
+                for i in range(n_single):
                     singles[i].replay()
             e1.record(stream)
         torch.cuda.synchronize()
@@ -552,9 +559,10 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e2e_steps // L):
+        n_whole, n_single = replay_plan(e2e_steps, L)
+        for _ in range(n_whole):
             e2e_whole.replay()
-        for i in range(e2e_steps % L):
+        for i in range(n_single):
             e2e_graphs[i].replay()
         e1.record(stream)
         stream.synchronize()
@@ -698,9 +706,10 @@ def _timed_steps(torch, stream, graphs, steps, warmup=3, per_step_graphs=False):
             for i in range(steps):
                 singles[i % len(singles)].replay()
         else:
-            for i in range(steps // GROUP):
+            n_group, n_single = replay_plan(steps, GROUP)
+            for i in range(n_group):
                 groups[i % len(groups)].replay()
-            for i in range(steps % GROUP):
+            for i in range(n_single):
                 singles[i % len(singles)].replay()
         e1.record(stream)
     torch.cuda.synchronize()

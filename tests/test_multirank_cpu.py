@@ -75,3 +75,14 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     bench.reference_arm(Args, "long", 1 << 20)
     assert called == [] and capsys.readouterr().out == ""
+
+
+def test_replay_plan_times_exactly_k_steps():
+    """The bench replays graphs of several steps: the group and one-step
+    replays it plans add up to exactly the K steps it reports, for every K."""
+    bench = _bench()
+    for group in (1, 3, 8):
+        for k in range(0, 100):
+            n_group, n_single = bench.replay_plan(k, group)
+            assert n_group * group + n_single == k
+            assert 0 <= n_single < group
