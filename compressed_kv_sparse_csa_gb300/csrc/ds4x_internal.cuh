@@ -159,7 +159,7 @@ struct AttnBatch {
   const uint16_t *q;
   uint16_t *out;
   float *lse;
-  bool q_shared;   // every item reads the one query at q (dense tiles)
+  bool q_shared;   // every item reads the one query at q (the window path's two row sets)
   float *out_f32;  // item b's normalised fp32 output at out_f32 + b * 64 * 512 instead of out (for a finalize)
 };
 cudaError_t launch_attn_batch(const AttnBatch &ab, int batch, void *ws, cudaStream_t stream);
