@@ -10,7 +10,7 @@ Formats (DS4X README, "Packed cache ABI"; element formats as named there):
 * Indexer row, 68 bytes = 128 E2M1 codes, two per byte (64 bytes)
                         + 4 UE8M0 scales, one per 32-value block.
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent:
 
 * field order inside a row is the order the page lists the fields in;
 * the even element of a pair sits in the low nibble of its byte;
