@@ -776,6 +776,11 @@ __global__ void __launch_bounds__(DS4X_TOPK_MAX) window_prep_kernel(const uint8_
                                                                     const uint8_t *ring_rows, int32_t ring_pos,
                                                                     int32_t w, int32_t *__restrict__ idx2,
                                                                     const uint8_t **ptrs, int64_t *lens) {
+  // launched as a programmatic dependent: the previous kernel (the scorer that
+  // wrote idx, or the previous call's finalize, which reads this workspace) is
+  // complete past this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j = threadIdx.x;
   idx2[j] = j < k ? idx[j] : -1;
   idx2[DS4X_TOPK_MAX + j] = j < w ? (ring_pos - j + DS4X_RING_ROWS) % DS4X_RING_ROWS : -1;
@@ -801,9 +806,8 @@ cudaError_t launch_window_attn(const uint8_t *kv_rows, int64_t n_rows, const int
   int32_t *idx2 = reinterpret_cast<int32_t *>(base + L.idx);
   const uint8_t **ptrs = reinterpret_cast<const uint8_t **>(base + L.ptrs);
   int64_t *lens = reinterpret_cast<int64_t *>(base + L.lens);
-  window_prep_kernel<<<1, DS4X_TOPK_MAX, 0, stream>>>(kv_rows, n_rows, idx, k, ring_rows, ring_pos, w, idx2, ptrs,
-                                                      lens);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(window_prep_kernel, 1u, unsigned(DS4X_TOPK_MAX), 0, stream, kv_rows, n_rows, idx, k,
+                             ring_rows, ring_pos, w, idx2, ptrs, lens);
   if (e != cudaSuccess) return e;
   AttnBatch ab{};
   ab.kv_arr = ptrs;
